@@ -1,0 +1,291 @@
+"""Pins for the fp64 oracle against facts it does not compute itself:
+closed forms, invariants, brute force on tiny inputs, an independent library
+routine, and the numbers printed on the mtrt.cn DeepSeek-Coder-V2 MLA page.
+Each test is chosen so that a plausible slip (a dropped term, a wrong sign or
+index, a transposed operand, a missing scale) fails it."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import mla_inputs as mi
+from oracle import mla_oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------- bf16
+def test_bf16_ties_and_single_rounding():
+    one = O.f64_to_bf16(np.array([1.0]))[0]
+    assert one == 0x3F80
+    # midpoint between 1 and 1+2^-7 -> even (1.0)
+    assert O.f64_to_bf16(np.array([1 + 2.0 ** -8]))[0] == 0x3F80
+    # midpoint between 1+2^-7 (odd) and 1+2^-6 (even) -> 1+2^-6
+    assert O.f64_to_bf16(np.array([1 + 3 * 2.0 ** -8]))[0] == 0x3F82
+    # just above the first midpoint: must round up; rounding through float32
+    # first would lose the 2^-40 and land on the tie (a double-rounding slip)
+    assert O.f64_to_bf16(np.array([1 + 2.0 ** -8 + 2.0 ** -40]))[0] == 0x3F81
+    assert O.f64_to_bf16(np.array([-2.0]))[0] == 0xC000
+    assert O.bf16_to_f64(np.array([0x3F81], np.uint16))[0] == 1 + 2.0 ** -7
+
+
+def test_bf16_matches_torch_on_float32_inputs():
+    rng = np.random.default_rng(5)
+    x = (rng.standard_normal(200000) * np.exp(rng.uniform(-20, 20, 200000))).astype(np.float32)
+    ours = O.f64_to_bf16(x.astype(np.float64))
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ours, ref)
+
+
+# ---------------------------------------------------------------- E4M3
+def test_e4m3_code_values_from_the_format_definition():
+    dec = O.e4m3_to_f64(np.arange(256, dtype=np.uint8))
+    assert dec[0x38] == 1.0 and dec[0x7E] == 448.0 and dec[0xC0] == -2.0
+    assert dec[0x01] == 2.0 ** -9 and dec[0x08] == 2.0 ** -6 and dec[0x07] == 7 * 2.0 ** -9
+    assert dec[0x00] == 0.0 and np.signbit(dec[0x80])
+    assert np.isnan(dec[0x7F]) and np.isnan(dec[0xFF])
+    assert np.sum(np.isnan(dec)) == 2
+    fin = [c for c in range(256) if c not in (0x7F, 0xFF)]
+    # every finite code is +-2^(e-7)(1+m/8) or a subnormal m/8 * 2^-6
+    for c in fin:
+        e, m = (c >> 3) & 0xF, c & 7
+        mag = (m / 8) * 2.0 ** -6 if e == 0 else (1 + m / 8) * 2.0 ** (e - 7)
+        assert abs(dec[c]) == mag
+    # encode(decode(c)) == c for every finite code
+    assert np.array_equal(O.f32_to_e4m3(dec[fin].astype(np.float32)), np.array(fin, np.uint8))
+
+
+def test_e4m3_rounding_ties_saturation():
+    enc = lambda v: int(O.f32_to_e4m3(np.array([v], np.float32))[0])
+    assert enc(1.0625) == 0x38          # tie between 0x38 (even) and 0x39
+    assert enc(1.1875) == 0x3A          # tie between 0x39 (odd) and 0x3A
+    assert enc(1.0625 + 1e-6) == 0x39   # above the tie
+    assert enc(2.0 ** -10) == 0x00      # subnormal tie -> even (zero)
+    assert enc(3 * 2.0 ** -10) == 0x02  # tie between 0x01 and 0x02
+    assert enc(1000.0) == 0x7E and enc(-1e6) == 0xFE and enc(448.0) == 0x7E
+    assert enc(460.0) == 0x7E
+    assert enc(float("nan")) == 0x7F
+
+
+def test_e4m3_matches_torch_in_range():
+    rng = np.random.default_rng(7)
+    x = (rng.standard_normal(300000) * np.exp(rng.uniform(-12, 6, 300000))).astype(np.float32)
+    x = x[np.abs(x) <= 448]
+    ours = O.f32_to_e4m3(x)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ours, ref)
+
+
+# ---------------------------------------------------------------- RMSNorm / RoPE
+def test_rmsnorm_closed_forms():
+    y = O.rmsnorm(np.array([[3.0, 4.0]]))
+    assert np.allclose(y, [[3 / math.sqrt(12.5), 4 / math.sqrt(12.5)]], rtol=0, atol=1e-15)
+    x = np.random.default_rng(1).standard_normal((4, 512))
+    assert np.allclose(np.mean(O.rmsnorm(x) ** 2, axis=1), 1.0, atol=1e-13)
+    assert np.allclose(O.rmsnorm(7.5 * x), O.rmsnorm(x), atol=1e-14)
+    assert np.allclose(O.rmsnorm(np.full((1, 8), -2.0)), -1.0)
+
+
+def test_rope_closed_forms_and_invariants():
+    e0 = np.zeros(64); e0[0] = 1.0
+    r = O.rope(e0, 1)
+    assert math.isclose(r[0], math.cos(1.0), abs_tol=1e-15)
+    assert math.isclose(r[32], math.sin(1.0), abs_tol=1e-15)
+    assert np.count_nonzero(np.abs(r) > 1e-15) == 2
+    e33 = np.zeros(64); e33[33] = 1.0
+    a = 7 * 10000.0 ** (-1 / 32)
+    r = O.rope(e33, 7)
+    assert math.isclose(r[1], -math.sin(a), abs_tol=1e-14)
+    assert math.isclose(r[33], math.cos(a), abs_tol=1e-14)
+    x = np.random.default_rng(2).standard_normal((5, 64))
+    assert np.array_equal(O.rope(x, 0), x)
+    pos = np.array([0, 1, 100, 4095, 131071])
+    assert np.allclose(np.linalg.norm(O.rope(x, pos), axis=1), np.linalg.norm(x, axis=1), rtol=1e-13)
+    assert np.allclose(O.rope(O.rope(x, 3), 5), O.rope(x, 8), atol=1e-12)
+    q, k = x[0], x[1]
+    d1 = O.rope(q, 50) @ O.rope(k, 20)
+    d2 = O.rope(q, 1030) @ O.rope(k, 1000)
+    assert math.isclose(d1, d2, rel_tol=1e-10, abs_tol=1e-10)
+
+
+# ---------------------------------------------------------------- attention
+def _tiny(B=2, H=4, lens=(65, 130), seed=11, pages="permuted"):
+    w = mi.Workload("t", B=B, H=H, L=0, ragged=(1, 2), seed=seed, pages=pages)
+    inp = mi.make_inputs(w, with_kv=False)
+    inp["seq_lens"] = np.array(lens, np.int32)
+    inp["page_table"], inp["num_pages"] = mi.page_layout(w, inp["seq_lens"])
+    inp["kv_raw"] = {b: mi.kv_rows(w, b, int(lens[b])) for b in range(B)}
+    return inp
+
+
+def test_absorbed_equals_non_absorbed():
+    inp = _tiny(B=3, lens=(1, 63, 130))
+    cache = O.build_cache(inp)
+    qpe = O.rope_q_bf16(inp["q_pe_raw"], inp["seq_lens"])
+    a, lse_a = O.decode_reference(cache, inp, qpe)
+    b, _, lse_b = O.decode_absorbed(cache, inp, qpe)
+    assert np.max(np.abs(a - b)) <= 1e-10 * np.max(np.abs(a))
+    assert np.allclose(lse_a, lse_b, rtol=0, atol=1e-10)
+
+
+def test_brute_force_triple_loop():
+    rng = np.random.default_rng(3)
+    n = 5
+    c = rng.standard_normal((n, 512)); kp = rng.standard_normal((n, 64))
+    qn = rng.standard_normal(128); qp = rng.standard_normal(64)
+    wuk = rng.standard_normal((128, 512)) / 20; wuv = rng.standard_normal((128, 512)) / 20
+    out, lse, p = O.decode_head(c, kp, qn, qp, wuk, wuv)
+    scores = []
+    for t in range(n):
+        k = [sum(wuk[i][j] * c[t][j] for j in range(512)) for i in range(128)] + list(kp[t])
+        q = list(qn) + list(qp)
+        scores.append(sum(q[i] * k[i] for i in range(192)) / math.sqrt(192))
+    mx = max(scores)
+    ex = [math.exp(s - mx) for s in scores]
+    tot = sum(ex)
+    ref = [0.0] * 128
+    for t in range(n):
+        for i in range(128):
+            ref[i] += ex[t] / tot * sum(wuv[i][j] * c[t][j] for j in range(512))
+    assert np.allclose(out, ref, rtol=1e-12, atol=1e-12)
+    assert math.isclose(lse, mx + math.log(tot), rel_tol=1e-13)
+    assert math.isclose(float(np.sum(p)), 1.0, abs_tol=1e-12)
+
+
+def test_score_scale_and_both_key_parts_closed_form():
+    # latent part: W_UK row 3 picks latent column 3; only token 0 has it
+    wuk = np.zeros((128, 512)); wuk[3, 3] = 1.0
+    wuv = np.random.default_rng(4).standard_normal((128, 512))
+    c = np.zeros((2, 512)); c[0, 3] = 1.0; c[1, 100] = 1.0
+    kp = np.zeros((2, 64)); kp[1, 5] = 1.0
+    qn = np.zeros(128); qn[3] = 2.0
+    qp = np.zeros(64); qp[5] = -1.5
+    out, _, p = O.decode_head(c, kp, qn, qp, wuk, wuv)
+    s0, s1 = 2.0 / math.sqrt(192), -1.5 / math.sqrt(192)
+    p0 = 1 / (1 + math.exp(s1 - s0))
+    assert math.isclose(p[0], p0, rel_tol=1e-14)
+    assert np.allclose(out, p0 * wuv[:, 3] + (1 - p0) * wuv[:, 100], rtol=1e-13, atol=1e-13)
+
+
+def test_one_token_context_returns_value_of_that_token():
+    inp = _tiny(B=1, lens=(1,))
+    cache = O.build_cache(inp)
+    qpe = O.rope_q_bf16(inp["q_pe_raw"], inp["seq_lens"])
+    out, _ = O.decode_reference(cache, inp, qpe)
+    c0, _ = O.gather_sequence(cache, inp["page_table"], 0, 1)
+    for h in range(inp["workload"].H):
+        assert np.allclose(out[h], O.bf16_to_f64(inp["w_uv"][h]) @ c0[0], rtol=1e-13, atol=1e-15)
+
+
+def test_zero_query_gives_mean_of_values():
+    inp = _tiny(B=1, lens=(77,))
+    inp["q_nope"] = np.zeros_like(inp["q_nope"])
+    cache = O.build_cache(inp)
+    qpe = np.zeros_like(inp["q_pe_raw"])
+    out, lse = O.decode_reference(cache, inp, qpe)
+    c, _ = O.gather_sequence(cache, inp["page_table"], 0, 77)
+    for h in range(inp["workload"].H):
+        assert np.allclose(out[h], O.bf16_to_f64(inp["w_uv"][h]) @ c.mean(axis=0), rtol=1e-12, atol=1e-14)
+    assert np.allclose(lse, math.log(77), atol=1e-13)
+
+
+def test_page_table_permutation_invariance_bit_exact():
+    inp = _tiny(B=2, lens=(200, 129), pages="contiguous")
+    cache = O.build_cache(inp)
+    qpe = O.rope_q_bf16(inp["q_pe_raw"], inp["seq_lens"])
+    ref, _ = O.decode_reference(cache, inp, qpe)
+    perm = np.random.default_rng(9).permutation(inp["num_pages"]).astype(np.int32)
+    inv = np.argsort(perm)
+    moved = dict(cache)
+    moved["ckv"], moved["kpe"] = cache["ckv"][inv], cache["kpe"][inv]
+    inp2 = dict(inp)
+    inp2["page_table"] = np.where(inp["page_table"] >= 0, perm[np.maximum(inp["page_table"], 0)], -1)
+    got, _ = O.decode_reference(moved, inp2, qpe)
+    assert np.array_equal(got, ref)
+
+
+def test_split_ranges_combine_by_lse_to_the_full_result():
+    inp = _tiny(B=1, lens=(300,))
+    cache = O.build_cache(inp)
+    qpe = O.bf16_to_f64(O.rope_q_bf16(inp["q_pe_raw"], inp["seq_lens"]))
+    qlat = O.absorb_q(inp["q_nope"], inp["w_uk"])
+    full, lse_full = O.latent_attention_range(cache, inp["page_table"], 0, 0, 300, qlat[0, 1], qpe[0, 1])
+    parts = [O.latent_attention_range(cache, inp["page_table"], 0, a, b, qlat[0, 1], qpe[0, 1])
+             for a, b in [(0, 64), (64, 65), (65, 300)]]
+    m = max(l for _, l in parts)
+    w = np.array([math.exp(l - m) for _, l in parts])
+    comb = sum(wi * o for wi, (o, _) in zip(w, parts)) / w.sum()
+    assert np.allclose(comb, full, rtol=1e-12, atol=1e-13)
+    assert math.isclose(m + math.log(w.sum()), lse_full, rel_tol=1e-13)
+
+
+# ---------------------------------------------------------------- cache write
+def test_cache_rows_norm_rope_and_slot_mapping():
+    inp = _tiny(B=2, lens=(70, 3))
+    cache = O.build_cache(inp)
+    c, kp = O.gather_sequence(cache, inp["page_table"], 0, 70)
+    assert np.allclose(np.mean(c ** 2, axis=1), 1.0, atol=2e-2)
+    raw = O.bf16_to_f64(inp["kv_raw"][0])
+    # position 0: the rotation is the identity, so the stored k_pe is the raw one
+    assert np.array_equal(kp[0], raw[0, 512:])
+    assert np.allclose(kp[69], O.rope(raw[69, 512:], 69), rtol=0, atol=2e-2)
+    # slot mapping: token 65 of sequence 0 sits in slot 1 of its second page
+    pg = inp["page_table"][0, 1]
+    assert np.array_equal(cache["ckv"][pg, 1], O.f64_to_bf16(O.rmsnorm(raw[65:66, :512]))[0])
+
+
+def test_e4m3_row_quantisation_error_bound():
+    inp = _tiny(B=1, lens=(128,))
+    cache = O.build_cache(inp, "e4m3")
+    bf = O.build_cache(inp)
+    t = np.arange(128)
+    pg, sl = inp["page_table"][0, t // 64], t % 64
+    c8, k8 = O.cache_values(cache, pg, sl)
+    c, k = O.cache_values(bf, pg, sl)
+    v8, v = np.concatenate([c8, k8], 1), np.concatenate([c, k], 1)
+    scale = cache["scale"][pg, sl][:, None].astype(np.float64)
+    # 3 mantissa bits: half an ulp is 2^-4 relative; subnormals 2^-10 absolute
+    err = np.abs(v8 - v)
+    assert np.all(err <= np.maximum(2.0 ** -4 * np.abs(v), 2.0 ** -10 * scale) * (1 + 1e-6))
+    # the largest value of each row maps to the top code
+    amax_code = np.max(np.concatenate([cache["ckv"][pg, sl], cache["kpe"][pg, sl]], 1) & 0x7F, axis=1)
+    assert np.all(amax_code == 0x7E)
+    z, s = O.quantize_rows_e4m3(np.zeros((1, 576), np.uint16))
+    assert s[0] == 1.0 and not z.any()
+
+
+# ---------------------------------------------------------------- accounting
+def test_cache_accounting_against_page_table():
+    g = json.load(open(os.path.join(GOLDEN, "p3_cache_table.json")))
+    acc = O.cache_accounting(heads=g["heads"], d_k=g["k_per_head"], d_v=g["v_per_head"],
+                             layers=g["layers"], tokens=g["context_tokens"],
+                             bytes_per=g["bytes_per_value_bf16"])
+    assert acc["mha_values_per_token_layer"] == g["printed_mha_values_per_token_layer"] == 32768
+    assert acc["mla_values_per_token_layer"] == g["printed_mla_values_per_token_layer"] == 576
+    assert g["printed_latent"] + g["printed_rope"] == 576
+    assert acc["mla_total_bytes"] == 9_059_696_640
+    assert acc["mha_total_bytes"] == 515_396_075_520
+    assert math.isclose(acc["ratio"], 56.888, rel_tol=1e-4)
+    # the page's printed totals (1.87 TB, 1.75 GB, >1000x) are not reachable
+    # from its own counts: recorded, not asserted as truth
+    assert abs(acc["mla_total_bytes"] - 1.75e9) > 1e9
+    assert acc["ratio"] < 1000
+
+
+# ---------------------------------------------------------------- generator
+def test_inputs_are_seeded_and_shaped():
+    a = mi.make_inputs(mi.WORKLOADS["tiny"])
+    b = mi.make_inputs(mi.WORKLOADS["tiny"])
+    assert np.array_equal(a["q_nope"], b["q_nope"]) and np.array_equal(a["kv_raw"][0], b["kv_raw"][0])
+    assert a["q_nope"].shape == (1, 16, 128) and a["w_uk"].shape == (16, 128, 512)
+    assert a["kv_raw"][0].shape == (512, 576) and a["num_pages"] == 8
+    w = O.bf16_to_f64(a["w_uk"])
+    assert abs(np.var(w) * 512 - 1.0) < 0.05
+    lens = mi.seq_lens_for(mi.WORKLOADS["ragged"])
+    assert lens.min() >= 1024 and lens.max() <= 32768 and len(lens) == 64
+    t, n = mi.page_layout(mi.WORKLOADS["ragged"], lens)
+    used = t[t >= 0]
+    assert n == int(np.sum((lens + 63) // 64)) and np.array_equal(np.sort(used), np.arange(n))
