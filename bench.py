@@ -1,0 +1,344 @@
+"""Benchmark of one MLA decode step (absorb -> latent attention with split-KV
+-> combine -> out-projection) on synthetic inputs of the DeepSeek-V2 layer
+shape: B=32 sequences, H=128 heads, 4096 cached tokens each, 576-d bf16
+latent cache in 64-token pages.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload v2_layer|tiny|long_ctx|ragged|fp8_batch]
+
+Prints one JSON line.  The L2 is flushed (a 256 MiB write) before every timed
+step; the step itself is timed with CUDA events on the launching stream.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import mla_inputs as mi  # noqa: E402
+
+METRIC = "MLA decode tokens/s and latent-cache HBM GB/s (% of ~8 TB/s roofline), 1 B300"
+FLUSH_BYTES = 256 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="v2_layer", choices=sorted(mi.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return d["hbm_gbs"], d["bf16_tflops"], "measured"
+    return 6400.0, 1800.0, "fallback"
+
+
+def cache_bytes_per_token(kv_dtype):
+    return 576 * 2 if kv_dtype == "bf16" else 576 + 4
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            self.proc.wait()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx = max(mx, float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx or None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- ours
+def setup_gpu(w, device):
+    import torch
+    import mla_latent_kv_66_b300 as mla
+    from mla_latent_kv_66_b300 import _lib as L
+
+    inp = mi.make_inputs(w, with_kv=False)
+    table, lens = inp["page_table"], inp["seq_lens"]
+    npg = inp["num_pages"]
+    p = L.make_params(w.B, w.H, table.shape[1], npg, w.kv_dtype, w.out_dtype)
+
+    def bf(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+
+    if w.kv_dtype == "e4m3":
+        ckv = torch.zeros(npg, 64, 512, dtype=torch.uint8, device=device)
+        kpe = torch.zeros(npg, 64, 64, dtype=torch.uint8, device=device)
+        sc = torch.ones(npg, 64, dtype=torch.float32, device=device)
+    else:
+        ckv = torch.zeros(npg, 64, 512, dtype=torch.bfloat16, device=device)
+        kpe = torch.zeros(npg, 64, 64, dtype=torch.bfloat16, device=device)
+        sc = None
+    for b in range(w.B):  # write the cache with the library's append kernel
+        n = int(lens[b])
+        t = np.arange(n)
+        slots = torch.from_numpy((table[b, t // 64].astype(np.int64) * 64 + t % 64).astype(np.int32)).to(device)
+        mla.mla_cache_append(p, bf(mi.kv_rows(w, b, n)), slots,
+                             torch.from_numpy(t.astype(np.int32)).to(device), 3, ckv, kpe, sc)
+    lens_d = torch.from_numpy(lens).to(device)
+    q_pe = torch.empty(w.B, w.H, 64, dtype=torch.bfloat16, device=device)
+    mla.mla_rope_q(p, bf(inp["q_pe_raw"]), lens_d, q_pe)
+    state = dict(inp=inp, p=p, ckv=ckv, kpe=kpe, sc=sc, lens=lens_d,
+                 table=torch.from_numpy(table).to(device), q_nope=bf(inp["q_nope"]), q_pe=q_pe,
+                 w_uk=bf(inp["w_uk"]), w_uv=bf(inp["w_uv"]))
+    step = mla.MLADecodeStep(w.B, w.H, table.shape[1], npg, w.kv_dtype, w.out_dtype, w.splits, device)
+    torch.cuda.synchronize()
+    return state, step
+
+
+def run_ours(args, w, rank, world):
+    import torch
+    import torch.distributed as dist
+    from mla_latent_kv_66_b300 import _lib as L
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    st, step = setup_gpu(w, dev)
+    p, G = step.p, step.num_splits
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    args_step = (st["q_nope"], st["q_pe"], st["w_uk"], st["w_uv"], st["ckv"], st["kpe"], st["sc"],
+                 st["table"], st["lens"])
+
+    def one(ev=None):
+        L.mla_absorb_q(p, st["q_nope"], st["w_uk"], step.q_lat)
+        if ev:
+            ev[0].record()
+        L.mla_decode(p, step.q_lat, st["q_pe"], st["ckv"], st["kpe"], st["sc"], st["table"], st["lens"], G,
+                     step.workspace, step.o_lat, step.lse)
+        if ev:
+            ev[1].record()
+        L.mla_split_kv_combine(p, step.workspace, G, step.o_lat, step.lse)
+        L.mla_out_proj(p, step.o_lat, st["w_uv"], step.out)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        one()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    K = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+            torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    with ClockSampler(dev.index) as clk:
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        wall0 = time.perf_counter()
+        for i in range(K):
+            flush.zero_()
+            a, b, c, d = evs[i]
+            a.record()
+            one((b, c))
+            d.record()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        wall = time.perf_counter() - wall0
+    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    dec_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    ms = statistics.mean(step_ms)
+    dms = statistics.mean(dec_ms)
+    if world > 1:
+        t = torch.tensor([ms, dms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, dms = t.tolist()
+
+    # end to end: pinned host inputs in, result out, through the public step call
+    inp = st["inp"]
+    host = {k: st[k].cpu().pin_memory() for k in ("q_nope", "q_pe", "table", "lens")}
+    devb = {k: torch.empty_like(st[k]) for k in host}
+    out_h = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+    e2e_ms = []
+    for i in range(max(3, args.warmup) + min(K, 500)):
+        flush.zero_()
+        a, d = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for k in host:
+            devb[k].copy_(host[k], non_blocking=True)
+        step(devb["q_nope"], devb["q_pe"], st["w_uk"], st["w_uv"], st["ckv"], st["kpe"], st["sc"],
+             devb["table"], devb["lens"])
+        out_h.copy_(step.out, non_blocking=True)
+        d.record()
+        d.synchronize()
+        if i >= max(3, args.warmup):
+            e2e_ms.append(a.elapsed_time(d))
+    e2e = statistics.mean(e2e_ms)
+    if world > 1:
+        t = torch.tensor([e2e], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e = t.item()
+    status = step.status()
+    return dict(ms=ms, dec_ms=dms, e2e_ms=e2e, h2d=h2d, d2h=d2h, wall=wall, clocks=clk.summary(),
+                status=status, G=G, tokens=int(inp["seq_lens"].sum()))
+
+
+# --------------------------------------------------------------------------- oracle (CPU)
+def cpu_oracle_sample(w, budget_s=15.0, seed=0):
+    """Time the fp64 oracle on a bounded sample of (sequence, head) pairs of
+    the same workload; returns (tokens/s, cores, description)."""
+    from threadpoolctl import threadpool_info
+    from oracle import mla_oracle as O
+
+    lens = mi.seq_lens_for(w)
+    rng = np.random.default_rng(seed)
+    b = int(rng.integers(w.B))
+    sub_w = mi.Workload("sample", B=1, H=w.H, L=int(lens[b]), seed=w.seed, kv_dtype=w.kv_dtype)
+    full = mi.make_inputs(w, seqs=[b])
+    n = int(lens[b])
+    table = np.arange((n + 63) // 64, dtype=np.int32)[None, :]
+    sub = {"workload": sub_w, "seq_lens": np.array([n], np.int32), "page_table": table,
+           "num_pages": table.shape[1], "q_nope": full["q_nope"][[b]], "q_pe_raw": full["q_pe_raw"][[b]],
+           "w_uk": full["w_uk"], "w_uv": full["w_uv"], "kv_raw": {0: full["kv_raw"][b]}}
+    cache = O.build_cache(sub, w.kv_dtype)
+    qpe = O.rope_q_bf16(sub["q_pe_raw"], sub["seq_lens"])
+    t0 = time.perf_counter()
+    heads = 0
+    while heads < w.H:
+        O.decode_reference(cache, sub, qpe, [(0, heads)])
+        heads += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+    tok_s = (heads / w.H) / dt  # one decoded token = all H heads of one sequence
+    return tok_s, threads, f"{heads} of {w.H} heads of sequence {b} (L={n}), non-absorbed fp64 oracle, {dt:.1f} s"
+
+
+def run_reference(args, w):
+    vals = []
+    for i in range(max(1, args.warmup) + args.steps):
+        v, cores, desc = cpu_oracle_sample(w, budget_s=max(1.0, 20.0 / max(1, args.steps)), seed=i)
+        if i >= max(1, args.warmup):
+            vals.append(v)
+    v = statistics.mean(vals)
+    return v, cores, desc
+
+
+# --------------------------------------------------------------------------- main
+def main():
+    args = parse()
+    w = mi.WORKLOADS[args.workload]
+    rank, world = int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+    cfg = {"workload": w.name, "B": w.B, "H": w.H, "L": w.L or "log-uniform[%d,%d]" % w.ragged,
+           "kv_lora_rank": 512, "rope_dim": 64, "page_size": 64, "kv_dtype": w.kv_dtype,
+           "pages": w.pages, "l2": "flushed before every timed step (256 MiB write)",
+           "parallelism": "replicas" if world > 1 else "single-gpu"}
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        v, cores, desc = run_reference(args, w)
+        print(json.dumps({"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s",
+                          "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                          "ms_per_step": 1000.0 * 1.0 / v if v else None, "higher_is_better": True,
+                          "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                          "config": cfg,
+                          "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                           "sample": desc},
+                          "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                                  "d2h_bytes_per_step": 0}}), flush=True)
+        return
+
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    r = run_ours(args, w, rank, world)
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+    hbm, tflops, src = peaks()
+    tokens_per_step = w.B
+    value = world * tokens_per_step / (r["ms"] / 1000.0)
+    cache_bytes = r["tokens"] * cache_bytes_per_token(w.kv_dtype)
+    achieved = cache_bytes / (r["dec_ms"] / 1000.0) / 1e9
+    cpu = None
+    if not args.no_cpu_baseline:
+        v, cores, desc = cpu_oracle_sample(w)
+        cpu = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc}
+    out = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": r["ms"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if w.kv_dtype == "bf16" else "e4m3-cache/bf16",
+        "data": "synthetic (seeded, DeepSeek-V2 MLA shapes; random-init weights)", "config": cfg,
+        "cache_gbs": achieved, "cache_bytes_per_step": cache_bytes,
+        "cached_tokens_per_s": r["tokens"] / (r["dec_ms"] / 1000.0),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": None, "kernel": "mla_decode",
+                     "peak_source": src, "decode_ms": r["dec_ms"]},
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * tokens_per_step / (r["e2e_ms"] / 1000.0), "unit": "tokens/s",
+                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+        "gpu_launches": 4 * args.steps,
+        "clocks": r["clocks"], "status": r["status"], "num_splits": r["G"], "wall_s_timed": r["wall"],
+    }
+    print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

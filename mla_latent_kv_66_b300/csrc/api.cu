@@ -1,0 +1,216 @@
+// Host side of the libmla C ABI: argument checks, workspace layout, the
+// choice of KV partition count, and kernel launches.
+#include <math.h>
+#include <string.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace mla;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+int g_sm_count[kMaxDevices];  // cached device property, 0 = not queried yet
+
+int sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  if (g_sm_count[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    g_sm_count[dev] = n;
+  }
+  return g_sm_count[dev];
+}
+
+mla_status check_params(const mla_params* p) {
+  if (!p) return MLA_ERR_INVALID_ARG;
+  if (p->B < 1 || p->H < 1 || p->max_pages_per_seq < 1 || p->num_pages < 1)
+    return MLA_ERR_INVALID_ARG;
+  if (!(p->softmax_scale > 0.f) || !isfinite(p->softmax_scale)) return MLA_ERR_INVALID_ARG;
+  if (p->kv_dtype != MLA_KV_BF16 && p->kv_dtype != MLA_KV_E4M3) return MLA_ERR_INVALID_ARG;
+  if (p->out_dtype != MLA_OUT_F32 && p->out_dtype != MLA_OUT_BF16) return MLA_ERR_INVALID_ARG;
+  if (p->kv_lora_rank != kLatent || p->rope_dim != kRope || p->nope_dim != kNope ||
+      p->v_dim != kV || p->page_size != kPage)
+    return MLA_ERR_UNSUPPORTED;
+  if (p->H % 16 != 0 || p->H > 128) return MLA_ERR_UNSUPPORTED;
+  if ((long long)p->num_pages * kPage > 0x7fffffffLL) return MLA_ERR_UNSUPPORTED;
+  if ((long long)p->B * p->max_pages_per_seq > 0x7fffffffLL) return MLA_ERR_UNSUPPORTED;
+  return MLA_OK;
+}
+
+int resolve_splits(int num_splits) {
+  if (num_splits < 0) return -1;
+  if (num_splits > 0) return num_splits <= 65536 ? num_splits : -1;
+  const int sms = sm_count();
+  return sms > 1 ? sms / 2 : 1;
+}
+
+mla_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* mla_status_string(mla_status s) {
+  switch (s) {
+    case MLA_OK: return "ok";
+    case MLA_ERR_INVALID_ARG: return "invalid argument";
+    case MLA_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case MLA_ERR_CUDA: return "CUDA error";
+    case MLA_ERR_PAGE_OOB: return "page id out of range";
+    case MLA_ERR_WORKSPACE: return "workspace missing or too small";
+    case MLA_ERR_SEQ_LEN: return "sequence length out of range";
+  }
+  return "unknown status";
+}
+
+int mla_version(void) { return 100; }
+
+int mla_decode_num_splits(const mla_params* p, int num_splits) {
+  if (check_params(p) != MLA_OK) return -1;
+  return resolve_splits(num_splits);
+}
+
+void mla_workspace_offsets(const mla_params* p, int num_splits, size_t offsets[5]) {
+  const int G = mla_decode_num_splits(p, num_splits);
+  if (G < 1 || !offsets) {
+    if (offsets) memset(offsets, 0, 5 * sizeof(size_t));
+    return;
+  }
+  WsLayout l = ws_layout(p->B, p->H, G);
+  offsets[0] = l.err;
+  offsets[1] = l.rec;
+  offsets[2] = l.seq_start;
+  offsets[3] = l.part_lse;
+  offsets[4] = l.part_o;
+}
+
+size_t mla_decode_workspace_size(const mla_params* p, int num_splits) {
+  const int G = mla_decode_num_splits(p, num_splits);
+  if (G < 1) return 0;
+  return ws_layout(p->B, p->H, G).total;
+}
+
+mla_status mla_absorb_q(const mla_params* p, const void* q_nope, const void* w_uk, void* q_lat,
+                        mla_stream_t stream) {
+  mla_status s = check_params(p);
+  if (s != MLA_OK) return s;
+  if (!q_nope || !w_uk || !q_lat) return MLA_ERR_INVALID_ARG;
+  return cuda_status(launch_absorb_simt(static_cast<const __nv_bfloat16*>(q_nope),
+                                        static_cast<const __nv_bfloat16*>(w_uk),
+                                        static_cast<__nv_bfloat16*>(q_lat), p->B, p->H,
+                                        (cudaStream_t)stream));
+}
+
+mla_status mla_decode(const mla_params* p, const void* q_lat, const void* q_pe,
+                      const void* ckv_cache, const void* kpe_cache, const float* kv_scale,
+                      const int32_t* page_table, const int32_t* seq_lens, int num_splits,
+                      void* workspace, size_t ws_bytes, void* o_lat, float* lse,
+                      mla_stream_t stream) {
+  mla_status s = check_params(p);
+  if (s != MLA_OK) return s;
+  if (!q_lat || !q_pe || !ckv_cache || !kpe_cache || !page_table || !seq_lens || !o_lat)
+    return MLA_ERR_INVALID_ARG;
+  const bool fp8 = p->kv_dtype == MLA_KV_E4M3;
+  if (fp8 != (kv_scale != nullptr)) return MLA_ERR_INVALID_ARG;
+  const int G = resolve_splits(num_splits);
+  if (G < 1) return MLA_ERR_INVALID_ARG;
+  const WsLayout l = ws_layout(p->B, p->H, G);
+  if (!workspace || ws_bytes < l.total) return MLA_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  DecodeArgs a;
+  a.q_lat = static_cast<const __nv_bfloat16*>(q_lat);
+  a.q_pe = static_cast<const __nv_bfloat16*>(q_pe);
+  a.ckv = ckv_cache;
+  a.kpe = kpe_cache;
+  a.kv_scale = kv_scale;
+  a.page_table = page_table;
+  a.seq_lens = seq_lens;
+  a.o_lat = static_cast<__nv_bfloat16*>(o_lat);
+  a.lse = lse;
+  a.err = reinterpret_cast<int*>(ws + l.err);
+  a.rec = reinterpret_cast<int4*>(ws + l.rec);
+  a.seq_start = reinterpret_cast<int*>(ws + l.seq_start);
+  a.part_lse = reinterpret_cast<float*>(ws + l.part_lse);
+  a.part_o = reinterpret_cast<float*>(ws + l.part_o);
+  a.B = p->B;
+  a.H = p->H;
+  a.G = G;
+  a.maxp = p->max_pages_per_seq;
+  a.num_pages = p->num_pages;
+  a.scale_log2 = p->softmax_scale * kLog2e;
+  return cuda_status(launch_decode_simt(a, (cudaStream_t)stream));
+}
+
+mla_status mla_split_kv_combine(const mla_params* p, const void* workspace, size_t ws_bytes,
+                                int num_splits, void* o_lat, float* lse, mla_stream_t stream) {
+  mla_status s = check_params(p);
+  if (s != MLA_OK) return s;
+  if (!o_lat) return MLA_ERR_INVALID_ARG;
+  const int G = resolve_splits(num_splits);
+  if (G < 1) return MLA_ERR_INVALID_ARG;
+  const WsLayout l = ws_layout(p->B, p->H, G);
+  if (!workspace || ws_bytes < l.total) return MLA_ERR_WORKSPACE;
+  const uint8_t* ws = static_cast<const uint8_t*>(workspace);
+  return cuda_status(launch_combine(reinterpret_cast<const float*>(ws + l.part_o),
+                                    reinterpret_cast<const float*>(ws + l.part_lse),
+                                    reinterpret_cast<const int*>(ws + l.seq_start),
+                                    static_cast<__nv_bfloat16*>(o_lat), lse, p->B, p->H, G,
+                                    (cudaStream_t)stream));
+}
+
+mla_status mla_out_proj(const mla_params* p, const void* o_lat, const void* w_uv, void* out,
+                        mla_stream_t stream) {
+  mla_status s = check_params(p);
+  if (s != MLA_OK) return s;
+  if (!o_lat || !w_uv || !out) return MLA_ERR_INVALID_ARG;
+  return cuda_status(launch_out_proj_simt(static_cast<const __nv_bfloat16*>(o_lat),
+                                          static_cast<const __nv_bfloat16*>(w_uv), out,
+                                          p->out_dtype == MLA_OUT_BF16, p->B, p->H,
+                                          (cudaStream_t)stream));
+}
+
+mla_status mla_cache_append(const mla_params* p, const void* kv_rows, const int32_t* slots,
+                            const int32_t* positions, int T, int flags, void* ckv_cache,
+                            void* kpe_cache, float* kv_scale, mla_stream_t stream) {
+  mla_status s = check_params(p);
+  if (s != MLA_OK) return s;
+  if (T < 0 || (flags & ~(MLA_APPEND_RMSNORM | MLA_APPEND_ROPE))) return MLA_ERR_INVALID_ARG;
+  if (T == 0) return MLA_OK;
+  if (!kv_rows || !slots || !ckv_cache || !kpe_cache) return MLA_ERR_INVALID_ARG;
+  if ((flags & MLA_APPEND_ROPE) && !positions) return MLA_ERR_INVALID_ARG;
+  const bool fp8 = p->kv_dtype == MLA_KV_E4M3;
+  if (fp8 && !kv_scale) return MLA_ERR_INVALID_ARG;
+  return cuda_status(launch_cache_append(static_cast<const __nv_bfloat16*>(kv_rows), slots,
+                                         positions, T, flags, fp8,
+                                         (long long)p->num_pages * kPage, ckv_cache, kpe_cache,
+                                         kv_scale, (cudaStream_t)stream));
+}
+
+mla_status mla_rope_q(const mla_params* p, const void* q_pe_raw, const int32_t* seq_lens,
+                      void* q_pe, mla_stream_t stream) {
+  mla_status s = check_params(p);
+  if (s != MLA_OK) return s;
+  if (!q_pe_raw || !seq_lens || !q_pe) return MLA_ERR_INVALID_ARG;
+  return cuda_status(launch_rope_q(static_cast<const __nv_bfloat16*>(q_pe_raw), seq_lens,
+                                   static_cast<__nv_bfloat16*>(q_pe), p->B, p->H,
+                                   (cudaStream_t)stream));
+}
+
+mla_status mla_workspace_status(void* workspace, int clear, mla_stream_t stream) {
+  if (!workspace) return MLA_ERR_INVALID_ARG;
+  int v = 0;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemcpyAsync(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MLA_ERR_CUDA;
+  if (clear && v != 0) {
+    if (cudaMemsetAsync(workspace, 0, sizeof(int), st) != cudaSuccess) return MLA_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return MLA_ERR_CUDA;
+  }
+  return (mla_status)v;
+}
+
+}  // extern "C"

@@ -1,0 +1,20 @@
+// Launch functions of the libmla kernels (internal to the library).
+#pragma once
+#include "common.cuh"
+
+namespace mla {
+
+cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_combine(const float* part_o, const float* part_lse, const int* seq_start,
+                           __nv_bfloat16* o_lat, float* lse, int B, int H, int G, cudaStream_t stream);
+cudaError_t launch_absorb_simt(const __nv_bfloat16* q_nope, const __nv_bfloat16* w_uk,
+                               __nv_bfloat16* q_lat, int B, int H, cudaStream_t stream);
+cudaError_t launch_out_proj_simt(const __nv_bfloat16* o_lat, const __nv_bfloat16* w_uv, void* out,
+                                 bool out_bf16, int B, int H, cudaStream_t stream);
+cudaError_t launch_cache_append(const __nv_bfloat16* rows, const int32_t* slots, const int32_t* pos,
+                                int T, int flags, bool fp8, long long num_slots, void* ckv,
+                                void* kpe, float* scale, cudaStream_t stream);
+cudaError_t launch_rope_q(const __nv_bfloat16* q_raw, const int32_t* seq_lens, __nv_bfloat16* q,
+                          int B, int H, cudaStream_t stream);
+
+}  // namespace mla

@@ -1,0 +1,36 @@
+"""One MLA decode step over a resident paged latent cache, through the C ABI:
+absorb the query (W_UK), latent attention with split-KV, combine, and the
+value out-projection (W_UV).  Buffers are allocated once, at construction."""
+from __future__ import annotations
+
+import torch
+
+from . import _lib as L
+
+
+class MLADecodeStep:
+    def __init__(self, B, H, max_pages_per_seq, num_pages, kv_dtype="bf16", out_dtype="f32",
+                 num_splits=0, device="cuda"):
+        self.p = L.make_params(B, H, max_pages_per_seq, num_pages, kv_dtype, out_dtype)
+        self.num_splits = L.mla_decode_num_splits(self.p, num_splits)
+        if self.num_splits < 1:
+            raise L.MLAError(L.MLA_ERR_INVALID_ARG, "MLADecodeStep")
+        ws = L.mla_decode_workspace_size(self.p, self.num_splits)
+        self.workspace = torch.zeros(ws, dtype=torch.uint8, device=device)
+        self.q_lat = torch.empty(B, H, 512, dtype=torch.bfloat16, device=device)
+        self.o_lat = torch.empty(B, H, 512, dtype=torch.bfloat16, device=device)
+        self.lse = torch.empty(B, H, dtype=torch.float32, device=device)
+        odt = torch.bfloat16 if out_dtype == "bf16" else torch.float32
+        self.out = torch.empty(B, H, 128, dtype=odt, device=device)
+
+    def __call__(self, q_nope, q_pe, w_uk, w_uv, ckv, kpe, kv_scale, page_table, seq_lens, stream=None):
+        p, G = self.p, self.num_splits
+        L.mla_absorb_q(p, q_nope, w_uk, self.q_lat, stream)
+        L.mla_decode(p, self.q_lat, q_pe, ckv, kpe, kv_scale, page_table, seq_lens, G,
+                     self.workspace, self.o_lat, self.lse, stream)
+        L.mla_split_kv_combine(p, self.workspace, G, self.o_lat, self.lse, stream)
+        L.mla_out_proj(p, self.o_lat, w_uv, self.out, stream)
+        return self.out
+
+    def status(self, clear=False):
+        return L.mla_workspace_status(self.workspace, clear)

@@ -1,0 +1,345 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle on the
+same seeded inputs.
+
+Tolerances (the contract for this path): bf16 cache
+max|out - ref| <= 1e-2 * max|ref| + 1e-3; FP8 cache against the oracle on the
+unquantised cache <= 5e-2 * max|ref|; page-table and split indexing bit-exact.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import mla_inputs as mi
+import mla_latent_kv_66_b300 as mla
+from mla_latent_kv_66_b300 import _lib as L
+from oracle import mla_oracle as O
+
+from helpers import (bf16_bits, bf16_dev, i32_dev, reference_partition, sample_pairs, tol_ok,
+                     to_f64, upload_cache)
+
+pytestmark = pytest.mark.gpu
+
+TOL_REL, TOL_ABS = 1e-2, 1e-3
+
+
+def small_inputs(lens, H=16, seed=21, pages="permuted"):
+    w = mi.Workload("t", B=len(lens), H=H, L=0, ragged=(1, 2), seed=seed, pages=pages)
+    inp = mi.make_inputs(w, with_kv=False)
+    inp["seq_lens"] = np.asarray(lens, np.int32)
+    inp["page_table"], inp["num_pages"] = mi.page_layout(w, inp["seq_lens"])
+    inp["kv_raw"] = {b: mi.kv_rows(w, b, int(lens[b])) for b in range(len(lens))}
+    return inp
+
+
+def garbage(inp, nan_tail=False):
+    g = mi.garbage_pool_bits(inp["workload"], inp["num_pages"], 512), \
+        mi.garbage_pool_bits(inp["workload"], inp["num_pages"], 64)
+    if nan_tail:
+        g = tuple(np.where(np.arange(x.shape[1])[None, :, None] % 2 == 1, np.uint16(0x7FC0), x) for x in g)
+    return g
+
+
+def run_gpu(inp, cache, q_pe_bits, num_splits, q_lat_bits=None, out_dtype="f32"):
+    w = inp["workload"]
+    B, H = len(inp["seq_lens"]), w.H
+    table = inp["page_table"]
+    p = L.make_params(B, H, table.shape[1], inp["num_pages"], cache["kv_dtype"], out_dtype)
+    G = L.mla_decode_num_splits(p, num_splits)
+    ws = torch.zeros(L.mla_decode_workspace_size(p, G), dtype=torch.uint8, device="cuda")
+    ckv, kpe, sc = upload_cache(cache)
+    qn, wuk, wuv = bf16_dev(inp["q_nope"]), bf16_dev(inp["w_uk"]), bf16_dev(inp["w_uv"])
+    qpe = bf16_dev(q_pe_bits)
+    tab, lens = i32_dev(table), i32_dev(inp["seq_lens"])
+    q_lat = torch.empty(B, H, 512, dtype=torch.bfloat16, device="cuda")
+    L.mla_absorb_q(p, qn, wuk, q_lat)
+    q_used = bf16_dev(q_lat_bits) if q_lat_bits is not None else q_lat
+    o_lat = torch.full((B, H, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((B, H), float("nan"), dtype=torch.float32, device="cuda")
+    L.mla_decode(p, q_used, qpe, ckv, kpe, sc, tab, lens, G, ws, o_lat, lse)
+    L.mla_split_kv_combine(p, ws, G, o_lat, lse)
+    out = torch.empty(B, H, 128, dtype=torch.bfloat16 if out_dtype == "bf16" else torch.float32, device="cuda")
+    L.mla_out_proj(p, o_lat, wuv, out)
+    torch.cuda.synchronize()
+    st = L.mla_workspace_status(ws)
+    return dict(q_lat=q_lat, o_lat=o_lat, lse=lse, out=out, ws=ws, p=p, G=G, status=st)
+
+
+def oracle_all(inp, cache, q_pe_bits, pairs=None):
+    return O.decode_reference(cache, inp, q_pe_bits, pairs)
+
+
+# ------------------------------------------------------------------ tiny workload, every output
+def test_tiny_workload_end_to_end_all_heads():
+    inp = mi.make_inputs(mi.WORKLOADS["tiny"])
+    cache = O.build_cache(inp, garbage=garbage(inp))
+    qpe = O.rope_q_bf16(inp["q_pe_raw"], inp["seq_lens"])
+    r = run_gpu(inp, cache, qpe, num_splits=0)
+    assert r["status"] == 0
+    ref, lse_ref = oracle_all(inp, cache, qpe)
+    got = to_f64(r["out"]).reshape(-1, 128)
+    ok, err, bound = tol_ok(got, ref, TOL_REL, TOL_ABS)
+    assert ok, (err, bound)
+    # intermediates: q_lat within one bf16 rounding of the fp64 absorption
+    qref = O.absorb_q(inp["q_nope"], inp["w_uk"])
+    qgot = to_f64(r["q_lat"])
+    assert np.all(np.abs(qgot - qref) <= 2.0 ** -8 * np.abs(qref) + 1e-6 * np.abs(qref).max())
+    assert np.allclose(to_f64(r["lse"]).reshape(-1), lse_ref, rtol=0, atol=1e-3)
+
+
+@pytest.mark.parametrize("splits", [1, 3, 8, 64])
+def test_decode_kernel_on_exact_q_lat(splits):
+    inp = small_inputs([700, 64, 1, 130, 65])
+    cache = O.build_cache(inp, garbage=garbage(inp))
+    qpe = O.rope_q_bf16(inp["q_pe_raw"], inp["seq_lens"])
+    qlat_ref = O.absorb_q(inp["q_nope"], inp["w_uk"])
+    qlat_bits = O.f64_to_bf16(qlat_ref)
+    r = run_gpu(inp, cache, qpe, splits, q_lat_bits=qlat_bits)
+    assert r["status"] == 0
+    qp = O.bf16_to_f64(qpe)
+    ql = O.bf16_to_f64(qlat_bits)
+    got = to_f64(r["o_lat"])
+    for b in range(len(inp["seq_lens"])):
+        n = int(inp["seq_lens"][b])
+        c, kp = O.gather_sequence(cache, inp["page_table"], b, n)
+        for h in range(inp["workload"].H):
+            o_ref, lse_ref = O.latent_attention(c, kp, ql[b, h], qp[b, h])
+            ok, err, bound = tol_ok(got[b, h], o_ref, TOL_REL, TOL_ABS)
+            assert ok, (b, h, err, bound)
+            assert abs(float(r["lse"][b, h]) - lse_ref) < 1e-3
+
+
+def test_one_token_context_returns_the_cached_latent_exactly():
+    inp = small_inputs([1, 1, 1])
+    cache = O.build_cache(inp, garbage=garbage(inp))
+    qpe = O.rope_q_bf16(inp["q_pe_raw"], inp["seq_lens"])
+    r = run_gpu(inp, cache, qpe, 2)
+    for b in range(3):
+        pg = inp["page_table"][b, 0]
+        c0 = cache["ckv"][pg, 0]
+        for h in range(16):
+            assert np.array_equal(bf16_bits(r["o_lat"][b, h]), c0)
+
+
+def test_garbage_and_nan_past_sequence_end_are_ignored():
+    inp = small_inputs([70, 5, 127])
+    cache = O.build_cache(inp, garbage=garbage(inp, nan_tail=True))
+    qpe = O.rope_q_bf16(inp["q_pe_raw"], inp["seq_lens"])
+    r = run_gpu(inp, cache, qpe, 4)
+    ref, _ = oracle_all(inp, cache, qpe)
+    got = to_f64(r["out"]).reshape(-1, 128)
+    assert np.all(np.isfinite(got))
+    assert tol_ok(got, ref, TOL_REL, TOL_ABS)[0]
+
+
+# ------------------------------------------------------------------ split indexing, bit-exact
+@pytest.mark.parametrize("lens,G", [([700, 64, 1, 130, 65], 7), ([4096] * 3, 5), ([64] * 9, 4),
+                                    ([3000, 10, 2000], 64), ([1, 2, 3], 8)])
+def test_split_records_match_the_documented_partition(lens, G):
+    inp = small_inputs(lens)
+    cache = O.build_cache(inp)
+    qpe = O.rope_q_bf16(inp["q_pe_raw"], inp["seq_lens"])
+    r = run_gpu(inp, cache, qpe, G)
+    offs = L.mla_workspace_offsets(r["p"], G)
+    raw = r["ws"].cpu().numpy()
+    rec = raw[offs[1]: offs[1] + 2 * G * 16].view(np.int32).reshape(2 * G, 4)
+    start = raw[offs[2]: offs[2] + (len(lens) + 1) * 4].view(np.int32)
+    ref_rec, ref_start = reference_partition(inp["seq_lens"].tolist(), inp["page_table"].shape[1], G)
+    assert np.array_equal(start, np.array(ref_start, np.int32))
+    assert [tuple(x) for x in rec.tolist()] == ref_rec
+
+
+def test_page_permutation_is_bit_exact_for_a_fixed_schedule():
+    inp = small_inputs([300, 129, 64], pages="contiguous")
+    cache = O.build_cache(inp, garbage=garbage(inp))
+    qpe = O.rope_q_bf16(inp["q_pe_raw"], inp["seq_lens"])
+    r1 = run_gpu(inp, cache, qpe, 5)
+    perm = np.random.default_rng(4).permutation(inp["num_pages"]).astype(np.int32)
+    inv = np.argsort(perm)
+    moved = dict(cache)
+    moved["ckv"], moved["kpe"] = cache["ckv"][inv], cache["kpe"][inv]
+    inp2 = dict(inp)
+    inp2["page_table"] = np.where(inp["page_table"] >= 0, perm[np.maximum(inp["page_table"], 0)], -1)
+    r2 = run_gpu(inp2, moved, qpe, 5)
+    assert torch.equal(r1["o_lat"].view(torch.int16), r2["o_lat"].view(torch.int16))
+    assert torch.equal(r1["out"], r2["out"])
+
+
+def test_split_counts_agree_within_tolerance():
+    inp = small_inputs([2000, 777])
+    cache = O.build_cache(inp)
+    qpe = O.rope_q_bf16(inp["q_pe_raw"], inp["seq_lens"])
+    a = to_f64(run_gpu(inp, cache, qpe, 1)["out"])
+    b = to_f64(run_gpu(inp, cache, qpe, 41)["out"])
+    assert tol_ok(b, a, TOL_REL, TOL_ABS)[0]
+
+
+# ------------------------------------------------------------------ device-side error word
+def test_out_of_range_page_and_bad_length_set_the_error_word():
+    inp = small_inputs([200, 100])
+    cache = O.build_cache(inp)
+    qpe = O.rope_q_bf16(inp["q_pe_raw"], inp["seq_lens"])
+    bad = dict(inp)
+    bad["page_table"] = inp["page_table"].copy()
+    bad["page_table"][0, 1] = inp["num_pages"] + 5
+    r = run_gpu(bad, cache, qpe, 3)
+    assert r["status"] == L.MLA_ERR_PAGE_OOB
+    assert L.mla_workspace_status(r["ws"], clear=True) == L.MLA_ERR_PAGE_OOB
+    assert L.mla_workspace_status(r["ws"]) == 0
+    bad = dict(inp)
+    bad["seq_lens"] = np.array([0, 100], np.int32)
+    r = run_gpu(bad, cache, qpe, 3)
+    assert r["status"] == L.MLA_ERR_SEQ_LEN
+    # the valid sequence is still decoded correctly
+    ref, _ = oracle_all(inp, cache, qpe, [(1, h) for h in range(16)])
+    assert tol_ok(to_f64(r["out"][1]), ref, TOL_REL, TOL_ABS)[0]
+
+
+def test_host_rejects_bad_arguments_with_an_error():
+    p = L.make_params(1, 16, 1, 1)
+    x = torch.zeros(1, 16, 128, dtype=torch.bfloat16, device="cuda")
+    bad = L.make_params(1, 16, 1, 1)
+    bad.rope_dim = 32
+    with pytest.raises(mla.MLAError):
+        L.mla_absorb_q(bad, x, x, x)
+    with pytest.raises(mla.MLAError):
+        L.mla_out_proj(p, x, x, None)
+
+
+# ------------------------------------------------------------------ FP8 cache
+def test_fp8_cache_small():
+    inp = small_inputs([300, 64, 1, 129])
+    cache8 = O.build_cache(inp, "e4m3", garbage=garbage(inp))
+    cache = O.build_cache(inp, garbage=garbage(inp))
+    qpe = O.rope_q_bf16(inp["q_pe_raw"], inp["seq_lens"])
+    r = run_gpu(inp, cache8, qpe, 3, out_dtype="bf16")
+    assert r["status"] == 0
+    got = to_f64(r["out"]).reshape(-1, 128)
+    ref8, _ = oracle_all(inp, cache8, qpe)
+    assert tol_ok(got, ref8, TOL_REL, TOL_ABS)[0]
+    ref, _ = oracle_all(inp, cache, qpe)
+    assert tol_ok(got, ref, 5e-2)[0]
+
+
+# ------------------------------------------------------------------ cache write and query RoPE
+def test_cache_append_bf16_and_rope_q():
+    inp = small_inputs([300, 70])
+    w = inp["workload"]
+    rows = np.concatenate([inp["kv_raw"][b] for b in range(2)])
+    slots = np.concatenate([inp["page_table"][b, np.arange(n) // 64] * 64 + np.arange(n) % 64
+                            for b, n in enumerate(inp["seq_lens"])]).astype(np.int32)
+    pos = np.concatenate([np.arange(n) for n in inp["seq_lens"]]).astype(np.int32)
+    p = L.make_params(2, w.H, inp["page_table"].shape[1], inp["num_pages"])
+    ckv = torch.zeros(inp["num_pages"], 64, 512, dtype=torch.bfloat16, device="cuda")
+    kpe = torch.zeros(inp["num_pages"], 64, 64, dtype=torch.bfloat16, device="cuda")
+    L.mla_cache_append(p, bf16_dev(rows), i32_dev(slots), i32_dev(pos), 3, ckv, kpe)
+    ref = O.build_cache(inp)
+    got_c, got_k = bf16_bits(ckv), bf16_bits(kpe)
+    for g, r_ in ((got_c, ref["ckv"]), (got_k, ref["kpe"])):
+        d = np.abs(g.astype(np.int32) - r_.astype(np.int32))
+        assert d.max() <= 1 and np.mean(d == 0) > 0.999
+    qraw = bf16_dev(inp["q_pe_raw"])
+    q = torch.empty_like(qraw)
+    L.mla_rope_q(p, qraw, i32_dev(inp["seq_lens"]), q)
+    d = np.abs(bf16_bits(q).astype(np.int32) - O.rope_q_bf16(inp["q_pe_raw"], inp["seq_lens"]).astype(np.int32))
+    assert d.max() <= 1 and np.mean(d == 0) > 0.999
+
+
+def test_fp8_encoding_is_bit_exact_on_identical_rows():
+    inp = small_inputs([333])
+    ref = O.build_cache(inp)  # bf16 cache rows (normalised, rotated)
+    n = 333
+    t = np.arange(n)
+    pg, sl = inp["page_table"][0, t // 64], t % 64
+    rows = np.concatenate([ref["ckv"][pg, sl], ref["kpe"][pg, sl]], axis=1)
+    # add some extreme rows: zeros, tiny, huge, ties
+    extra = np.zeros((3, 576), np.uint16)
+    extra[1, :] = O.f64_to_bf16(np.full(576, 1e-30))
+    extra[2, :] = O.f64_to_bf16(np.linspace(-3e4, 3e4, 576))
+    rows = np.concatenate([rows, extra])
+    codes_ref, scale_ref = O.quantize_rows_e4m3(rows)
+    T = rows.shape[0]
+    npages = (T + 63) // 64
+    p = L.make_params(1, 16, npages, npages, "e4m3")
+    ckv = torch.zeros(npages, 64, 512, dtype=torch.uint8, device="cuda")
+    kpe = torch.zeros(npages, 64, 64, dtype=torch.uint8, device="cuda")
+    sc = torch.zeros(npages, 64, dtype=torch.float32, device="cuda")
+    L.mla_cache_append(p, bf16_dev(rows), i32_dev(np.arange(T)), i32_dev(np.zeros(T)), 0, ckv, kpe, sc)
+    got = np.concatenate([ckv.cpu().numpy().reshape(-1, 512)[:T], kpe.cpu().numpy().reshape(-1, 64)[:T]], 1)
+    assert np.array_equal(got, codes_ref)
+    assert np.array_equal(sc.cpu().numpy().reshape(-1)[:T], scale_ref)
+
+
+# ------------------------------------------------------------------ full-size workloads, sampled
+def build_gpu_cache(inp, kv_dtype):
+    """Write the whole workload's cache with the GPU append kernel."""
+    w = inp["workload"]
+    table, lens = inp["page_table"], inp["seq_lens"]
+    npg = inp["num_pages"]
+    p = L.make_params(w.B, w.H, table.shape[1], npg, kv_dtype)
+    if kv_dtype == "e4m3":
+        ckv = torch.full((npg, 64, 512), 0x44, dtype=torch.uint8, device="cuda")
+        kpe = torch.full((npg, 64, 64), 0x44, dtype=torch.uint8, device="cuda")
+        sc = torch.ones(npg, 64, dtype=torch.float32, device="cuda")
+    else:
+        ckv = torch.full((npg, 64, 512), 3.0, dtype=torch.bfloat16, device="cuda")
+        kpe = torch.full((npg, 64, 64), 3.0, dtype=torch.bfloat16, device="cuda")
+        sc = None
+    for b in range(w.B):
+        n = int(lens[b])
+        t = np.arange(n)
+        slots = (table[b, t // 64].astype(np.int64) * 64 + t % 64).astype(np.int32)
+        L.mla_cache_append(p, bf16_dev(mi.kv_rows(w, b, n)), i32_dev(slots), i32_dev(t),
+                           3, ckv, kpe, sc)
+    return ckv, kpe, sc
+
+
+def oracle_sampled(w, pairs):
+    """fp64 oracle on a compact sub-problem holding only the sampled sequences
+    (the result does not depend on where pages sit in the pool)."""
+    seqs = sorted({b for b, _ in pairs})
+    full = mi.make_inputs(w, seqs=seqs)
+    lens = full["seq_lens"][seqs]
+    npg = (lens + 63) // 64
+    table = np.full((len(seqs), int(npg.max())), -1, np.int32)
+    k = 0
+    for i, n in enumerate(npg):
+        table[i, :n] = np.arange(k, k + n)
+        k += int(n)
+    sub = {"workload": dataclasses.replace(w, B=len(seqs)), "seq_lens": lens, "page_table": table,
+           "num_pages": k, "q_nope": full["q_nope"][seqs], "q_pe_raw": full["q_pe_raw"][seqs],
+           "w_uk": full["w_uk"], "w_uv": full["w_uv"],
+           "kv_raw": {i: full["kv_raw"][b] for i, b in enumerate(seqs)}}
+    cache = O.build_cache(sub, w.kv_dtype)
+    qpe = O.rope_q_bf16(sub["q_pe_raw"], sub["seq_lens"])
+    return O.decode_reference(cache, sub, qpe, [(seqs.index(b), h) for b, h in pairs])
+
+
+@pytest.mark.parametrize("name,n_seq,n_head", [("v2_layer", 3, 3), ("long_ctx", 1, 3),
+                                               ("ragged", 3, 2), ("fp8_batch", 2, 2)])
+def test_full_size_workloads_sampled(name, n_seq, n_head):
+    w = mi.WORKLOADS[name]
+    inp = mi.make_inputs(w, with_kv=False)
+    ckv, kpe, sc = build_gpu_cache(inp, w.kv_dtype)
+    B, H = w.B, w.H
+    table = inp["page_table"]
+    p = L.make_params(B, H, table.shape[1], inp["num_pages"], w.kv_dtype, w.out_dtype)
+    step = mla.MLADecodeStep(B, H, table.shape[1], inp["num_pages"], w.kv_dtype, w.out_dtype, w.splits)
+    lens = i32_dev(inp["seq_lens"])
+    qpe = torch.empty(B, H, 64, dtype=torch.bfloat16, device="cuda")
+    L.mla_rope_q(p, bf16_dev(inp["q_pe_raw"]), lens, qpe)
+    out = step(bf16_dev(inp["q_nope"]), qpe, bf16_dev(inp["w_uk"]), bf16_dev(inp["w_uv"]),
+               ckv, kpe, sc, i32_dev(table), lens)
+    torch.cuda.synchronize()
+    assert step.status() == 0
+    pairs = sample_pairs(B, H, n_seq, n_head, seed=w.seed)
+    ref, lse_ref = oracle_sampled(w, pairs)
+    got = np.stack([to_f64(out[b, h]) for b, h in pairs])
+    if w.kv_dtype == "e4m3":
+        ok, err, bound = tol_ok(got, ref, 5e-2)
+    else:
+        ok, err, bound = tol_ok(got, ref, TOL_REL, TOL_ABS)
+    assert ok, (name, err, bound)
+    glse = np.array([float(step.lse[b, h]) for b, h in pairs])
+    assert np.allclose(glse, lse_ref, atol=2e-2 if w.kv_dtype == "e4m3" else 2e-3)
