@@ -50,7 +50,8 @@ typedef enum {
   MLA_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
   MLA_ERR_PAGE_OOB = 4,     /* a page id outside [0, num_pages) was seen */
   MLA_ERR_WORKSPACE = 5,    /* workspace missing or smaller than required */
-  MLA_ERR_SEQ_LEN = 6       /* a sequence length outside [1, max_pages*64] */
+  MLA_ERR_SEQ_LEN = 6,      /* a sequence length outside [1, max_pages*64] */
+  MLA_ERR_TIMEOUT = 7       /* a kernel gave up a bounded wait (internal fault) */
 } mla_status;
 
 typedef enum { MLA_KV_BF16 = 0, MLA_KV_E4M3 = 1 } mla_kv_dtype;

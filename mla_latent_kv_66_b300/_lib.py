@@ -16,7 +16,7 @@ import torch
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmla.so")
 
 MLA_OK, MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED, MLA_ERR_CUDA = 0, 1, 2, 3
-MLA_ERR_PAGE_OOB, MLA_ERR_WORKSPACE, MLA_ERR_SEQ_LEN = 4, 5, 6
+MLA_ERR_PAGE_OOB, MLA_ERR_WORKSPACE, MLA_ERR_SEQ_LEN, MLA_ERR_TIMEOUT = 4, 5, 6, 7
 MLA_KV_BF16, MLA_KV_E4M3 = 0, 1
 MLA_OUT_F32, MLA_OUT_BF16 = 0, 1
 MLA_APPEND_RMSNORM, MLA_APPEND_ROPE = 1, 2

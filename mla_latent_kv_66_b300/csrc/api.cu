@@ -40,11 +40,15 @@ mla_status check_params(const mla_params* p) {
   return MLA_OK;
 }
 
-int resolve_splits(int num_splits) {
+// 0 = automatic: one worker per pair of SMs, but never more workers than the
+// batch can have pages (B * max_pages_per_seq).
+int resolve_splits(const mla_params* p, int num_splits) {
   if (num_splits < 0) return -1;
   if (num_splits > 0) return num_splits <= 65536 ? num_splits : -1;
   const int sms = sm_count();
-  return sms > 1 ? sms / 2 : 1;
+  long long g = sms > 1 ? sms / 2 : 1;
+  const long long cap = (long long)p->B * p->max_pages_per_seq;
+  return (int)(g < cap ? g : cap);
 }
 
 mla_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA; }
@@ -62,6 +66,7 @@ const char* mla_status_string(mla_status s) {
     case MLA_ERR_PAGE_OOB: return "page id out of range";
     case MLA_ERR_WORKSPACE: return "workspace missing or too small";
     case MLA_ERR_SEQ_LEN: return "sequence length out of range";
+    case MLA_ERR_TIMEOUT: return "kernel wait timed out";
   }
   return "unknown status";
 }
@@ -70,7 +75,7 @@ int mla_version(void) { return 100; }
 
 int mla_decode_num_splits(const mla_params* p, int num_splits) {
   if (check_params(p) != MLA_OK) return -1;
-  return resolve_splits(num_splits);
+  return resolve_splits(p, num_splits);
 }
 
 void mla_workspace_offsets(const mla_params* p, int num_splits, size_t offsets[5]) {
@@ -98,7 +103,7 @@ mla_status mla_absorb_q(const mla_params* p, const void* q_nope, const void* w_u
   mla_status s = check_params(p);
   if (s != MLA_OK) return s;
   if (!q_nope || !w_uk || !q_lat) return MLA_ERR_INVALID_ARG;
-  return cuda_status(launch_absorb_simt(static_cast<const __nv_bfloat16*>(q_nope),
+  return cuda_status(launch_absorb_tc(static_cast<const __nv_bfloat16*>(q_nope),
                                         static_cast<const __nv_bfloat16*>(w_uk),
                                         static_cast<__nv_bfloat16*>(q_lat), p->B, p->H,
                                         (cudaStream_t)stream));
@@ -115,7 +120,7 @@ mla_status mla_decode(const mla_params* p, const void* q_lat, const void* q_pe,
     return MLA_ERR_INVALID_ARG;
   const bool fp8 = p->kv_dtype == MLA_KV_E4M3;
   if (fp8 != (kv_scale != nullptr)) return MLA_ERR_INVALID_ARG;
-  const int G = resolve_splits(num_splits);
+  const int G = resolve_splits(p, num_splits);
   if (G < 1) return MLA_ERR_INVALID_ARG;
   const WsLayout l = ws_layout(p->B, p->H, G);
   if (!workspace || ws_bytes < l.total) return MLA_ERR_WORKSPACE;
@@ -149,7 +154,7 @@ mla_status mla_split_kv_combine(const mla_params* p, const void* workspace, size
   mla_status s = check_params(p);
   if (s != MLA_OK) return s;
   if (!o_lat) return MLA_ERR_INVALID_ARG;
-  const int G = resolve_splits(num_splits);
+  const int G = resolve_splits(p, num_splits);
   if (G < 1) return MLA_ERR_INVALID_ARG;
   const WsLayout l = ws_layout(p->B, p->H, G);
   if (!workspace || ws_bytes < l.total) return MLA_ERR_WORKSPACE;
@@ -166,7 +171,7 @@ mla_status mla_out_proj(const mla_params* p, const void* o_lat, const void* w_uv
   mla_status s = check_params(p);
   if (s != MLA_OK) return s;
   if (!o_lat || !w_uv || !out) return MLA_ERR_INVALID_ARG;
-  return cuda_status(launch_out_proj_simt(static_cast<const __nv_bfloat16*>(o_lat),
+  return cuda_status(launch_out_proj_tc(static_cast<const __nv_bfloat16*>(o_lat),
                                           static_cast<const __nv_bfloat16*>(w_uv), out,
                                           p->out_dtype == MLA_OUT_BF16, p->B, p->H,
                                           (cudaStream_t)stream));

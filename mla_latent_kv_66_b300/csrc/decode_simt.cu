@@ -252,12 +252,14 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   if (wf == wl) return;  // finished by the decode kernel
   float mx = -INFINITY;
   for (int w = wf; w <= wl; ++w) {
+    if (range_lo(w + 1, G, P) == range_lo(w, G, P)) continue;  // empty range: no partial
     const int slot = sb <= range_lo(w, G, P) ? w : G + w;
     mx = fmaxf(mx, part_lse[(size_t)slot * H + h]);
   }
   float4 acc[4] = {};
   float sum = 0.f;
   for (int w = wf; w <= wl; ++w) {
+    if (range_lo(w + 1, G, P) == range_lo(w, G, P)) continue;
     const int slot = sb <= range_lo(w, G, P) ? w : G + w;
     const float l = part_lse[(size_t)slot * H + h];
     const float wt = l == -INFINITY ? 0.f : __expf(l - mx);

@@ -1,0 +1,195 @@
+// Query absorption and value out-projection on the tcgen05 tensor cores.
+//
+//   absorb:   q_lat[b,h,m] = sum_n W_UK[h,n,m] q_nope[b,h,n]   M=latent (4 tiles of 128), K=128
+//   out_proj: out[b,h,v]   = sum_k W_UV[h,v,k] o_lat[b,h,k]    M=v (128), K=512
+//
+// Both are the key and value halves of kv_b_proj (mtrt.cn DeepSeek-Coder-V2
+// MLA page, "KV 解压" step) applied on the query and output side.  Each CTA
+// computes one head's [128 x N] tile, N = the batch rounded up to 16, with
+// the batch as the MMA's N dimension; the weights stream once through a TMA
+// pipeline into 128-byte-swizzled shared memory, the accumulator lives in
+// tensor memory.  W_UK is read with its latent axis as M, i.e. as an
+// MN-major A operand; W_UV is K-major.
+#include "kernels.h"
+#include "tc.cuh"
+#include "tmap.cuh"
+
+namespace mla {
+namespace {
+
+using namespace tc;
+
+constexpr uint32_t kABytes = 16384;  // A bytes per 64-wide K block
+
+struct GemmTcArgs {
+  int B, H, N;
+  void* out;
+  int out_kind;  // 0: q_lat bf16 [B,H,512]; 1: out fp32 [B,H,128]; 2: out bf16 [B,H,128]
+};
+
+template <int kMode>
+__global__ void __launch_bounds__(128, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__ CUtensorMap tB,
+                   GemmTcArgs g) {
+  constexpr int KB = kMode == 0 ? 2 : 8;  // K blocks of 64
+  constexpr int S = kMode == 0 ? 2 : 4;   // pipeline stages
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bars[2 * S + 1];
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t b_bytes = (uint32_t)g.N * 128u;
+  const uint32_t stage = kABytes + b_bytes;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.x, mt = blockIdx.y, nt = blockIdx.z;
+  const uint32_t full = smem_u32(&bars[0]), empty = smem_u32(&bars[S]), done = smem_u32(&bars[2 * S]);
+  const uint32_t ncols = g.N <= 32 ? 32 : g.N <= 64 ? 64 : g.N <= 128 ? 128 : 256;
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int i = 0; i < S; ++i) {
+      mbar_init(full + 8 * i, 1);
+      mbar_init(empty + 8 * i, 1);
+    }
+    mbar_init(done, 1);
+    fence_mbar_init();
+    prefetch_tmap(&tA);
+    prefetch_tmap(&tB);
+  }
+  if (warp == 2) {
+    tmem_alloc(smem_u32(&tmem_slot), ncols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // TMA producer
+    int issued = 0;
+    for (int kb = 0; kb < KB; ++kb) {
+      const int s = kb % S;
+      if (kb >= S && !mbar_wait(empty + 8 * s, ((kb / S) - 1) & 1, &abort_flag, nullptr)) break;
+      const uint32_t a_s = base + s * stage, b_s = a_s + kABytes;
+      mbar_expect_tx(full + 8 * s, stage);
+      if (kMode == 0) {
+        tma_load_2d(a_s, &tA, full + 8 * s, mt * 128, h * 128 + kb * 64);
+        tma_load_2d(a_s + 8192, &tA, full + 8 * s, mt * 128 + 64, h * 128 + kb * 64);
+      } else {
+        tma_load_2d(a_s, &tA, full + 8 * s, kb * 64, h * 128);
+      }
+      tma_load_3d(b_s, &tB, full + 8 * s, kb * 64, h, nt * g.N);
+      ++issued;
+    }
+    if (abort_flag) {  // let copies in flight land before the CTA exits
+      for (int kb = issued - 1; kb >= 0 && kb >= issued - S; --kb) {
+        volatile int no_abort = 0;
+        mbar_wait(full + 8 * (kb % S), (kb / S) & 1, &no_abort, nullptr);
+      }
+    }
+  } else if (warp == 1 && lane == 0) {
+    // MMA issuer
+    const uint32_t idesc = idesc_bf16(128, g.N, kMode == 0, false);
+    for (int kb = 0; kb < KB; ++kb) {
+      const int s = kb % S;
+      if (!mbar_wait(full + 8 * s, (kb / S) & 1, &abort_flag, nullptr)) break;
+      tc_fence_after();
+      const uint32_t a_s = base + s * stage, b_s = a_s + kABytes;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        // MN-major A advances 16 K-rows (2 KB); K-major operands advance 32 B
+        const uint64_t ad = kMode == 0 ? sdesc_sw128(a_s + k * 2048, 8192, 1024)
+                                       : sdesc_sw128(a_s + k * 32, 16, 1024);
+        const uint64_t bd = sdesc_sw128(b_s + k * 32, 16, 1024);
+        mma_bf16_ss(tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+      }
+      mma_commit(empty + 8 * s);
+    }
+    mma_commit(done);
+  }
+  __syncwarp();
+
+  // epilogue: thread = accumulator row (TMEM lane), columns = batch
+  const bool ok = mbar_wait(done, 0, &abort_flag, nullptr) && !abort_flag;
+  tc_fence_after();
+  const int row = warp * 32 + lane;
+  for (int c0 = 0; c0 < g.N; c0 += 16) {
+    uint32_t r[16];
+    tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, r);
+    tmem_wait_ld();
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int b = nt * g.N + c0 + j;
+      if (b >= g.B) break;
+      const float v = ok ? __uint_as_float(r[j]) : __int_as_float(0x7fc00000);
+      const size_t bh = (size_t)b * g.H + h;
+      if (g.out_kind == 0)
+        static_cast<__nv_bfloat16*>(g.out)[bh * kLatent + mt * 128 + row] = __float2bfloat16_rn(v);
+      else if (g.out_kind == 1)
+        static_cast<float*>(g.out)[bh * kV + row] = v;
+      else
+        static_cast<__nv_bfloat16*>(g.out)[bh * kV + row] = __float2bfloat16_rn(v);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, ncols);
+  }
+}
+
+int batch_tile(int B) {
+  const int n = (B + 15) / 16 * 16;
+  return n < 256 ? n : 256;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+cudaError_t launch_absorb_tc(const __nv_bfloat16* q_nope, const __nv_bfloat16* w_uk,
+                             __nv_bfloat16* q_lat, int B, int H, cudaStream_t stream) {
+  if (!aligned16(q_nope) || !aligned16(w_uk)) return cudaErrorInvalidValue;
+  const int N = batch_tile(B);
+  CUtensorMap tA, tB;
+  const cuuint64_t ad[2] = {kLatent, (cuuint64_t)H * kNope}, as[1] = {kLatent * 2};
+  const cuuint32_t abox[2] = {64, 64};
+  const cuuint64_t bd[3] = {kNope, (cuuint64_t)H, (cuuint64_t)B},
+                   bs[2] = {kNope * 2, (cuuint64_t)H * kNope * 2};
+  const cuuint32_t bbox[3] = {64, 1, (cuuint32_t)N};
+  if (!make_tmap(&tA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w_uk, ad, as, abox) ||
+      !make_tmap(&tB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q_nope, bd, bs, bbox))
+    return cudaErrorInvalidValue;
+  GemmTcArgs g{B, H, N, q_lat, 0};
+  const size_t smem = 2 * (kABytes + (size_t)N * 128) + 1024;
+  cudaFuncSetAttribute(gemm_tc_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  dim3 grid(H, kLatent / 128, (B + N - 1) / N);
+  gemm_tc_kernel<0><<<grid, 128, smem, stream>>>(tA, tB, g);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_out_proj_tc(const __nv_bfloat16* o_lat, const __nv_bfloat16* w_uv, void* out,
+                               bool out_bf16, int B, int H, cudaStream_t stream) {
+  if (!aligned16(o_lat) || !aligned16(w_uv)) return cudaErrorInvalidValue;
+  const int N = batch_tile(B);
+  CUtensorMap tA, tB;
+  const cuuint64_t ad[2] = {kLatent, (cuuint64_t)H * kV}, as[1] = {kLatent * 2};
+  const cuuint32_t abox[2] = {64, 128};
+  const cuuint64_t bd[3] = {kLatent, (cuuint64_t)H, (cuuint64_t)B},
+                   bs[2] = {kLatent * 2, (cuuint64_t)H * kLatent * 2};
+  const cuuint32_t bbox[3] = {64, 1, (cuuint32_t)N};
+  if (!make_tmap(&tA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w_uv, ad, as, abox) ||
+      !make_tmap(&tB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, o_lat, bd, bs, bbox))
+    return cudaErrorInvalidValue;
+  GemmTcArgs g{B, H, N, out, out_bf16 ? 2 : 1};
+  const size_t smem = 4 * (kABytes + (size_t)N * 128) + 1024;
+  cudaFuncSetAttribute(gemm_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  dim3 grid(H, 1, (B + N - 1) / N);
+  gemm_tc_kernel<1><<<grid, 128, smem, stream>>>(tA, tB, g);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

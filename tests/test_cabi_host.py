@@ -32,7 +32,7 @@ def test_library_exports_every_declared_symbol():
 
 
 def test_status_strings():
-    for s in range(7):
+    for s in range(8):
         assert mla.status_string(s) and mla.status_string(s) != "unknown status"
     assert mla.status_string(99) == "unknown status"
 
