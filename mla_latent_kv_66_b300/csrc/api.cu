@@ -11,17 +11,23 @@ using namespace mla;
 namespace {
 
 constexpr int kMaxDevices = 64;
-int g_sm_count[kMaxDevices];  // cached device property, 0 = not queried yet
+int g_workers[kMaxDevices];  // cached device property, 0 = not queried yet
 
-int sm_count() {
+// Decode workers that run at once: co-resident clusters of the decode kernel
+// (one per pair of SMs where the GPCs allow it).
+int device_workers() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
-  if (g_sm_count[dev] == 0) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    g_sm_count[dev] = n;
+  if (g_workers[dev] == 0) {
+    int n = decode_tc_max_clusters();
+    if (n <= 0) {
+      int sms = 0;
+      if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+      n = sms / 2;
+    }
+    g_workers[dev] = n;
   }
-  return g_sm_count[dev];
+  return g_workers[dev];
 }
 
 mla_status check_params(const mla_params* p) {
@@ -40,13 +46,13 @@ mla_status check_params(const mla_params* p) {
   return MLA_OK;
 }
 
-// 0 = automatic: one worker per pair of SMs, but never more workers than the
+// 0 = automatic: one worker per co-resident decode cluster, but never more workers than the
 // batch can have pages (B * max_pages_per_seq).
 int resolve_splits(const mla_params* p, int num_splits) {
   if (num_splits < 0) return -1;
   if (num_splits > 0) return num_splits <= 65536 ? num_splits : -1;
-  const int sms = sm_count();
-  long long g = sms > 1 ? sms / 2 : 1;
+  const int nw = device_workers();
+  long long g = nw > 0 ? nw : 1;
   const long long cap = (long long)p->B * p->max_pages_per_seq;
   return (int)(g < cap ? g : cap);
 }
@@ -146,7 +152,8 @@ mla_status mla_decode(const mla_params* p, const void* q_lat, const void* q_pe,
   a.maxp = p->max_pages_per_seq;
   a.num_pages = p->num_pages;
   a.scale_log2 = p->softmax_scale * kLog2e;
-  return cuda_status(launch_decode_simt(a, (cudaStream_t)stream));
+  return cuda_status(fp8 ? launch_decode_simt(a, (cudaStream_t)stream)
+                         : launch_decode_tc(a, (cudaStream_t)stream));
 }
 
 mla_status mla_split_kv_combine(const mla_params* p, const void* workspace, size_t ws_bytes,

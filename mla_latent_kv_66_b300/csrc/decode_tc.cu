@@ -1,0 +1,547 @@
+// Latent-attention decode on the tcgen05 tensor cores (bf16 latent cache).
+//
+// Method (mtrt.cn DeepSeek-Coder-V2 MLA page, forward flow; absorbed form):
+//   s_t = scale * (q_lat . c_t + q_pe . k_pe_t),  o_lat = sum_t softmax(s)_t c_t
+// for all H <= 128 heads of one sequence at once: the heads are the M = 128
+// rows of every MMA, so each 64-token cache page is read from HBM once and
+// shared by all heads.
+//
+// The fp32 latent accumulator O[128 heads x 512] alone needs all 512 tensor
+// memory columns of an SM, so a cluster of two CTAs splits the latent axis:
+//   rank 0: latent columns [0,256);  rank 1: latent [256,512) and k_pe.
+// Each CTA TMA-loads only its part of every page and computes the partial
+// score over its part (rank 1 adds the shared RoPE key).  The two partial
+// score tiles are swapped through distributed shared memory and added in
+// both CTAs (fp32 addition commutes, so both see the same scores and make
+// the same softmax decisions); each CTA then accumulates P . c over its own
+// 256 latent columns.
+//
+// Warp roles (256 threads):
+//   warp 0      TMA producer (cache pages, 4-stage ring)
+//   warp 1      MMA issuer: S = Q K^T (A = query in tensor memory), O += P V
+//   warp 2      tensor-memory allocation
+//   warp 3      KV-partition schedule, split records
+//   warps 4..7  softmax: thread = head row; score swap, online softmax with
+//               lazy rescaling, P to shared memory, O rescale, epilogue
+// Tensor memory: O [0,256), S double buffer [256,384), query [384,512).
+#include "kernels.h"
+#include "tc.cuh"
+#include "tmap.cuh"
+
+namespace mla {
+namespace {
+
+using namespace tc;
+
+constexpr int kStages = 4;
+constexpr uint32_t kBox = 8192;             // [64 rows x 64 bf16], 128-byte swizzle
+constexpr uint32_t kStageBytes = 5 * kBox;  // 4 latent boxes + k_pe box (rank 1)
+constexpr uint32_t kOffQpe = kStages * kStageBytes;  // [128 x 64] bf16 (rank 1)
+constexpr uint32_t kOffP = kOffQpe + 16384;          // [128 x 64] bf16 probabilities
+constexpr uint32_t kOffX = kOffP + 16384;            // [128 x 64] fp32 peer partial scores
+constexpr uint32_t kSmemBytes = kOffX + 32768 + 1024;
+constexpr uint32_t kTmO = 0, kTmS = 256, kTmQ = 384;
+constexpr int kThreads = 256;
+constexpr float kRescaleLog2 = 8.f;  // lazy rescale threshold: P stays <= 2^8
+
+enum {
+  B_FULL = 0,
+  B_EMPTY = B_FULL + kStages,
+  B_SFULL = B_EMPTY + kStages,
+  B_SFREE = B_SFULL + 2,
+  B_XFULL = B_SFREE + 2,
+  B_XFREE,
+  B_PFULL,
+  B_PFREE,
+  B_ODONE,
+  B_OFREE,
+  B_QFULL,
+  B_QFREE,
+  B_IDLE,
+  B_COUNT
+};
+
+struct Unit {
+  int b, pb, pe, n, slot;
+  bool split, at_lo, at_hi;
+};
+
+// Walks the units of one worker range [lo, hi) of flattened pages.
+struct Walker {
+  int b;
+  long long sb, lo, hi;
+  int w, G;
+  __device__ bool next(const DecodeArgs& a, Unit& u) {
+    while (b < a.B && sb < hi) {
+      const int n = a.seq_lens[b];
+      const int np = seq_pages(n, a.maxp, nullptr);
+      const int bb = b;
+      const long long s0 = sb;
+      ++b;
+      sb += np;
+      if (np > 0) {
+        const long long ub = max(lo, s0), ue = min(hi, s0 + np);
+        u.b = bb;
+        u.n = n;
+        u.pb = (int)(ub - s0);
+        u.pe = (int)(ue - s0);
+        u.split = s0 < lo || s0 + np > hi;
+        u.at_lo = ub == lo;
+        u.at_hi = ue == hi;
+        u.slot = u.at_lo ? w : G + w;
+        return true;
+      }
+    }
+    return false;
+  }
+};
+
+__device__ inline uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ inline void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+__device__ inline float4 ld_shared_v4f(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    decode_tc_kernel(const __grid_constant__ CUtensorMap tm_ckv,
+                     const __grid_constant__ CUtensorMap tm_kpe, DecodeArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bars[B_COUNT];
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+  __shared__ long long sh_P, sh_s0;
+  __shared__ int sh_b0;
+
+  const uint32_t rank = cluster_rank(), peer = rank ^ 1u;
+  const int w = blockIdx.x >> 1;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(bar(B_FULL + i), 1);
+      mbar_init(bar(B_EMPTY + i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(B_SFULL + i), 1);
+      mbar_init(bar(B_SFREE + i), 128);
+    }
+    mbar_init(bar(B_XFULL), 128);
+    mbar_init(bar(B_XFREE), 128);
+    mbar_init(bar(B_PFULL), 128);
+    mbar_init(bar(B_PFREE), 1);
+    mbar_init(bar(B_ODONE), 1);
+    mbar_init(bar(B_OFREE), 128);
+    mbar_init(bar(B_QFULL), 128);
+    mbar_init(bar(B_QFREE), 1);
+    mbar_init(bar(B_IDLE), 1);
+    fence_mbar_init();
+    prefetch_tmap(&tm_ckv);
+    prefetch_tmap(&tm_kpe);
+  }
+  if (warp == 2) {
+    tmem_alloc(smem_u32(&tmem_slot), 512);
+    tmem_relinquish();
+  }
+  if (warp == 3) {
+    const bool lead = w == 0 && rank == 0;
+    const long long P = warp_total_pages(a.seq_lens, a.B, a.maxp, lead ? a.err : nullptr,
+                                         lead ? a.seq_start : nullptr);
+    const long long lo = range_lo(w, a.G, P), hi = range_lo(w + 1, a.G, P);
+    int b0 = a.B;
+    long long s0 = 0;
+    if (lo < hi) warp_find_seq(a.seq_lens, a.B, a.maxp, lo, &b0, &s0);
+    if (lane == 0) {
+      sh_P = P;
+      sh_b0 = b0;
+      sh_s0 = s0;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // barrier inits visible to the peer before any remote arrive
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  const long long P = sh_P;
+  const Walker walker0{sh_b0, sh_s0, range_lo(w, a.G, P), range_lo(w + 1, a.G, P), w, a.G};
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      Walker wk = walker0;
+      Unit u;
+      uint32_t g = 0;
+      bool ok = true;
+      const uint32_t tx = rank == 0 ? 4 * kBox : 5 * kBox;
+      while (ok && wk.next(a, u)) {
+        for (int j = u.pb; j < u.pe; ++j, ++g) {
+          const uint32_t s = g % kStages;
+          if (g >= kStages &&
+              !mbar_wait(bar(B_EMPTY + s), ((g / kStages) - 1) & 1, &abort_flag, a.err)) {
+            ok = false;
+            break;
+          }
+          int page = a.page_table[(size_t)u.b * a.maxp + j];
+          if (page < 0 || page >= a.num_pages) page = 0;  // masked by the softmax warps
+          const uint32_t st = base + s * kStageBytes;
+          mbar_expect_tx(bar(B_FULL + s), tx);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            tma_load_2d(st + i * kBox, &tm_ckv, bar(B_FULL + s), (int)rank * 256 + i * 64, page * kPage);
+          if (rank == 1) tma_load_2d(st + 4 * kBox, &tm_kpe, bar(B_FULL + s), 0, page * kPage);
+        }
+      }
+      // copies still in flight must land before the CTA can exit
+      for (uint32_t k = g > (uint32_t)kStages ? g - kStages : 0; k < g; ++k) {
+        volatile int no_abort = 0;
+        mbar_wait(bar(B_FULL + k % kStages), (k / kStages) & 1, &no_abort, nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      Walker wk = walker0;
+      Unit u;
+      uint32_t g = 0, uc = 0;
+      bool ok = true;
+      const uint32_t idesc_qk = idesc_bf16(128, 64, false, false);
+      const uint32_t idesc_pv = idesc_bf16(128, 256, false, true);
+      while (ok && wk.next(a, u)) {
+        const int np = u.pe - u.pb;
+        if (!mbar_wait(bar(B_QFULL), uc & 1, &abort_flag, a.err)) break;
+        tc_fence_after();
+        for (int i = 0; i <= np; ++i) {
+          if (i < np) {  // S = Q K^T for page g+i
+            const uint32_t gi = g + i, s = gi % kStages, sb = gi & 1;
+            if (!mbar_wait(bar(B_FULL + s), (gi / kStages) & 1, &abort_flag, a.err) ||
+                (gi >= 2 && !mbar_wait(bar(B_SFREE + sb), ((gi >> 1) - 1) & 1, &abort_flag, a.err))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t st = base + s * kStageBytes, d = tmem + kTmS + sb * 64;
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk)
+              mma_bf16_ts(d, tmem + kTmQ + kk * 8,
+                          sdesc_sw128(st + (kk >> 2) * kBox + (kk & 3) * 32, 16, 1024), idesc_qk,
+                          kk > 0 ? 1u : 0u);
+            if (rank == 1) {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                mma_bf16_ss(d, sdesc_sw128(base + kOffQpe + kk * 32, 16, 1024),
+                            sdesc_sw128(st + 4 * kBox + kk * 32, 16, 1024), idesc_qk, 1u);
+            }
+            mma_commit(bar(B_SFULL + sb));
+            if (i == np - 1) mma_commit(bar(B_QFREE));
+          }
+          if (i >= 1) {  // O += P V for page g+i-1
+            const uint32_t gp = g + i - 1, s = gp % kStages;
+            if (!mbar_wait(bar(B_PFULL), gp & 1, &abort_flag, a.err) ||
+                (i == 1 && uc >= 1 && !mbar_wait(bar(B_OFREE), (uc - 1) & 1, &abort_flag, a.err))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t st = base + s * kStageBytes;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_bf16_ss(tmem + kTmO, sdesc_sw128(base + kOffP + kk * 32, 16, 1024),
+                          sdesc_sw128(st + kk * 2048, kBox, 1024), idesc_pv,
+                          (i > 1 || kk > 0) ? 1u : 0u);
+            mma_commit(bar(B_PFREE));
+            mma_commit(bar(B_EMPTY + s));
+            if (i == np) mma_commit(bar(B_ODONE));
+          }
+        }
+        g += np;
+        ++uc;
+      }
+      mma_commit(bar(B_IDLE));  // every issued MMA has finished once this fires
+      volatile int no_abort = 0;
+      mbar_wait(bar(B_IDLE), 0, &no_abort, nullptr);
+    }
+  } else if (warp == 3) {
+    // ------------------------------------------------------------ split records
+    if (lane == 0 && rank == 0) {
+      Walker wk = walker0;
+      Unit u;
+      int4 first = make_int4(-1, 0, 0, 0), last = make_int4(-1, 0, 0, 0);
+      while (wk.next(a, u)) {
+        const int4 r = make_int4(u.b, u.pb, u.pe, u.split ? 1 : 0);
+        if (u.at_lo) first = r;
+        else if (u.at_hi) last = r;
+      }
+      a.rec[w] = first;
+      a.rec[a.G + w] = last;
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax warps
+    const int h = threadIdx.x - 128;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t x_peer = mapa(base + kOffX, peer);
+    const uint32_t xfull_peer = mapa(bar(B_XFULL), peer), xfree_peer = mapa(bar(B_XFREE), peer);
+    const float c = a.scale_log2;
+    const int H = a.H;
+
+    // every lane waits, then the warp agrees, so warp-collective operations
+    // never run with some lanes gone after an aborted wait
+    auto wwait = [&](int i, uint32_t parity) {
+      return __all_sync(0xffffffffu, mbar_wait(bar(i), parity, &abort_flag, a.err));
+    };
+    auto wwait_c = [&](int i, uint32_t parity) {
+      return __all_sync(0xffffffffu, mbar_wait<true>(bar(i), parity, &abort_flag, a.err));
+    };
+
+    auto load_q = [&](const Unit& q) {
+      // query latent half -> tensor memory (two bf16 per column); q_pe -> smem
+      const uint4* src = reinterpret_cast<const uint4*>(a.q_lat + ((size_t)q.b * H + h) * kLatent + rank * 256);
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t r[32];
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          uint4 x = h < H ? src[cc * 8 + v] : make_uint4(0, 0, 0, 0);
+          r[4 * v] = x.x;
+          r[4 * v + 1] = x.y;
+          r[4 * v + 2] = x.z;
+          r[4 * v + 3] = x.w;
+        }
+        tmem_st32(tmem + lane_base + kTmQ + cc * 32, r);
+      }
+      if (rank == 1) {
+        const uint4* sp = reinterpret_cast<const uint4*>(a.q_pe + ((size_t)q.b * H + h) * kRope);
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {
+          uint4 x = h < H ? sp[cc] : make_uint4(0, 0, 0, 0);
+          st_shared_v4(base + kOffQpe + h * 128 + ((cc ^ (h & 7)) * 16), x.x, x.y, x.z, x.w);
+        }
+      }
+      tmem_wait_st();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(B_QFULL));
+    };
+
+    Walker wk = walker0;
+    Unit u;
+    uint32_t g = 0, uc = 0;
+    bool ok = true;
+    bool have = wk.next(a, u);
+    if (have) load_q(u);
+    while (ok && have) {
+      const int np = u.pe - u.pb;
+      float m = -INFINITY, l = 0.f;
+      for (int i = 0; i < np; ++i) {
+        const uint32_t gi = g + i, sb = gi & 1, s = gi % kStages;
+        const int j = u.pb + i;
+        const int page = a.page_table[(size_t)u.b * a.maxp + j];
+        const bool page_ok = page >= 0 && page < a.num_pages;
+        if (!page_ok && h == 0 && rank == 0) set_error(a.err, MLA_ERR_PAGE_OOB);
+        const int valid = page_ok ? min(kPage, u.n - j * kPage) : 0;
+
+        // my partial scores
+        if (!wwait(B_SFULL + sb, (gi >> 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t s0[32], s1[32];
+        tmem_ld32(tmem + lane_base + kTmS + sb * 64, s0);
+        tmem_ld32(tmem + lane_base + kTmS + sb * 64 + 32, s1);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(bar(B_SFREE + sb));
+
+        // swap partial scores with the peer CTA
+        if (gi >= 1 && !wwait_c(B_XFREE, (gi - 1) & 1)) { ok = false; break; }
+        const uint32_t xrow = h * 256;
+#pragma unroll
+        for (int cc = 0; cc < 16; ++cc) {
+          const uint32_t* src = cc < 8 ? &s0[cc * 4] : &s1[(cc - 8) * 4];
+          st_cluster_v4(x_peer + xrow + ((cc ^ (h & 15)) * 16), src[0], src[1], src[2], src[3]);
+        }
+        mbar_arrive_remote(xfull_peer);
+        if (!wwait_c(B_XFULL, gi & 1)) { ok = false; break; }
+        float x[64];
+#pragma unroll
+        for (int cc = 0; cc < 16; ++cc) {
+          const float4 v = ld_shared_v4f(base + kOffX + xrow + ((cc ^ (h & 15)) * 16));
+          const uint32_t* own = cc < 8 ? &s0[cc * 4] : &s1[(cc - 8) * 4];
+          x[cc * 4 + 0] = __uint_as_float(own[0]) + v.x;
+          x[cc * 4 + 1] = __uint_as_float(own[1]) + v.y;
+          x[cc * 4 + 2] = __uint_as_float(own[2]) + v.z;
+          x[cc * 4 + 3] = __uint_as_float(own[3]) + v.w;
+        }
+        mbar_arrive_remote(xfree_peer);
+
+        // online softmax in the log2 domain, lazy rescaling
+        float mx = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < 64; ++k) {
+          x[k] = k < valid ? x[k] * c : -INFINITY;
+          mx = fmaxf(mx, x[k]);
+        }
+        float alpha = 1.f;
+        bool resc = false;
+        if (mx > m + kRescaleLog2) {
+          alpha = exp2f(m - mx);
+          resc = i > 0;
+          m = mx;
+        }
+        const float mm = m == -INFINITY ? 0.f : m;
+        float sum = 0.f;
+        uint32_t pk[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const float p0 = exp2f(x[2 * k] - mm), p1 = exp2f(x[2 * k + 1] - mm);
+          sum += p0 + p1;
+          pk[k] = pack_bf16(p0, p1);
+        }
+        l = l * alpha + sum;
+
+        // zero cache rows past the sequence end (garbage could be NaN)
+        if (valid < kPage) {
+          const uint32_t st = base + s * kStageBytes;
+          const int rows = kPage - valid, per_box = rows * 8;
+          for (int idx = h; idx < 4 * per_box; idx += 128) {
+            const int box = idx / per_box, rem = idx % per_box;
+            st_shared_v4(st + box * kBox + (valid + rem / 8) * 128 + (rem % 8) * 16, 0, 0, 0, 0);
+          }
+        }
+
+        // P buffer and O are free once the previous page's P V has finished
+        if (gi >= 1 && !wwait(B_PFREE, (gi - 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, resc)) {
+          const float f = resc ? alpha : 1.f;
+#pragma unroll 1
+          for (int cc = 0; cc < 8; ++cc) {
+            uint32_t r[32];
+            tmem_ld32(tmem + lane_base + kTmO + cc * 32, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * f);
+            tmem_st32(tmem + lane_base + kTmO + cc * 32, r);
+          }
+          tmem_wait_st();
+        }
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc)
+          st_shared_v4(base + kOffP + h * 128 + ((cc ^ (h & 7)) * 16), pk[4 * cc], pk[4 * cc + 1],
+                       pk[4 * cc + 2], pk[4 * cc + 3]);
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(bar(B_PFULL));
+      }
+      if (!ok) break;
+
+      // next unit's query can go in as soon as this unit's last S = Q K^T is done
+      Unit nu;
+      const bool have_next = wk.next(a, nu);
+      if (have_next) {
+        if (!wwait(B_QFREE, uc & 1)) break;
+        tc_fence_after();
+        load_q(nu);
+      }
+
+      // epilogue: normalise this CTA's 256 latent columns of every head row
+      if (!wwait(B_ODONE, uc & 1)) break;
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const size_t row = (size_t)u.b * H + h;
+      const size_t prow = (size_t)u.slot * H + h;
+#pragma unroll 1
+      for (int cc = 0; cc < 8; ++cc) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_base + kTmO + cc * 32, r);
+        tmem_wait_ld();
+        if (h < H) {
+          if (!u.split) {
+            uint4* dst = reinterpret_cast<uint4*>(a.o_lat + row * kLatent + rank * 256 + cc * 32);
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              dst[v] = make_uint4(pack_bf16(__uint_as_float(r[8 * v]) * inv, __uint_as_float(r[8 * v + 1]) * inv),
+                                  pack_bf16(__uint_as_float(r[8 * v + 2]) * inv, __uint_as_float(r[8 * v + 3]) * inv),
+                                  pack_bf16(__uint_as_float(r[8 * v + 4]) * inv, __uint_as_float(r[8 * v + 5]) * inv),
+                                  pack_bf16(__uint_as_float(r[8 * v + 6]) * inv, __uint_as_float(r[8 * v + 7]) * inv));
+          } else {
+            float4* dst = reinterpret_cast<float4*>(a.part_o + prow * kLatent + rank * 256 + cc * 32);
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              dst[v] = make_float4(__uint_as_float(r[4 * v]) * inv, __uint_as_float(r[4 * v + 1]) * inv,
+                                   __uint_as_float(r[4 * v + 2]) * inv, __uint_as_float(r[4 * v + 3]) * inv);
+          }
+        }
+      }
+      if (rank == 0 && h < H) {
+        const float lse = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+        if (!u.split) {
+          if (a.lse) a.lse[row] = lse;
+        } else {
+          a.part_lse[prow] = lse;
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar(B_OFREE));
+      g += np;
+      ++uc;
+      u = nu;
+      have = have_next;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // the peer no longer touches this CTA's shared memory
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+// Clusters of the decode kernel that fit on the device at once (0 on error).
+int decode_tc_max_clusters() {
+  if (cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kSmemBytes) != cudaSuccess)
+    return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, decode_tc_kernel, &cfg) != cudaSuccess) return 0;
+  return n;
+}
+
+cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t stream) {
+  if ((reinterpret_cast<uintptr_t>(a.ckv) & 15) || (reinterpret_cast<uintptr_t>(a.kpe) & 15))
+    return cudaErrorInvalidValue;
+  CUtensorMap tc_map, tk_map;
+  const cuuint64_t rows = (cuuint64_t)a.num_pages * kPage;
+  const cuuint64_t cd[2] = {kLatent, rows}, cs[1] = {kLatent * 2};
+  const cuuint64_t kd[2] = {kRope, rows}, ks[1] = {kRope * 2};
+  const cuuint32_t box[2] = {64, 64};
+  if (!make_tmap(&tc_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.ckv, cd, cs, box) ||
+      !make_tmap(&tk_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.kpe, kd, ks, box))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)kSmemBytes);
+  if (e != cudaSuccess) return e;
+  decode_tc_kernel<<<2 * a.G, kThreads, kSmemBytes, stream>>>(tc_map, tk_map, a);
+  return cudaGetLastError();
+}
+
+}  // namespace mla
