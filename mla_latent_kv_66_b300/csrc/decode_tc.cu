@@ -16,13 +16,19 @@
 // the same softmax decisions); each CTA then accumulates P . c over its own
 // 256 latent columns.
 //
-// Warp roles (256 threads):
-//   warp 0      TMA producer (cache pages, 4-stage ring)
-//   warp 1      MMA issuer: S = Q K^T (A = query in tensor memory), O += P V
-//   warp 2      tensor-memory allocation
-//   warp 3      KV-partition schedule, split records
-//   warps 4..7  softmax: thread = head row; score swap, online softmax with
-//               lazy rescaling, P to shared memory, O rescale, epilogue
+// Warp roles (384 threads):
+//   warp 0       TMA producer (cache pages, 3-stage ring)
+//   warp 1       MMA issuer for S = Q K^T (A = query in tensor memory)
+//   warp 2       tensor-memory allocation; then relays "exchange buffer
+//                consumed" to the peer CTA and re-arms the receive barrier
+//   warp 3       KV-partition schedule, split records; then MMA issuer for
+//                O += P V (a separate issuer lets S = Q K^T run ahead)
+//   warps 4..7   exchange: push each partial score tile to the peer CTA with
+//                asynchronous remote stores (st.async) as soon as its
+//                S = Q K^T completes; double-buffered
+//   warps 8..11  softmax: thread = head row; add the peer's partial, online
+//                softmax with lazy rescaling, P to shared memory, O rescale,
+//                per-unit epilogue
 // Tensor memory: O [0,256), S double buffer [256,384), query [384,512).
 #include "kernels.h"
 #include "tc.cuh"
@@ -33,15 +39,16 @@ namespace {
 
 using namespace tc;
 
-constexpr int kStages = 4;
+constexpr int kStages = 3;
 constexpr uint32_t kBox = 8192;             // [64 rows x 64 bf16], 128-byte swizzle
 constexpr uint32_t kStageBytes = 5 * kBox;  // 4 latent boxes + k_pe box (rank 1)
 constexpr uint32_t kOffQpe = kStages * kStageBytes;  // [128 x 64] bf16 (rank 1)
 constexpr uint32_t kOffP = kOffQpe + 16384;          // [128 x 64] bf16 probabilities
-constexpr uint32_t kOffX = kOffP + 16384;            // [128 x 64] fp32 peer partial scores
-constexpr uint32_t kSmemBytes = kOffX + 32768 + 1024;
+constexpr uint32_t kOffX = kOffP + 16384;            // 2 x [128 x 64] fp32 peer partial scores
+constexpr uint32_t kXBytes = 32768;
+constexpr uint32_t kSmemBytes = kOffX + 2 * kXBytes + 1024;
 constexpr uint32_t kTmO = 0, kTmS = 256, kTmQ = 384;
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
 constexpr float kRescaleLog2 = 8.f;  // lazy rescale threshold: P stays <= 2^8
 
 enum {
@@ -50,8 +57,9 @@ enum {
   B_SFULL = B_EMPTY + kStages,
   B_SFREE = B_SFULL + 2,
   B_XFULL = B_SFREE + 2,
-  B_XFREE,
-  B_PFULL,
+  B_XFREE = B_XFULL + 2,
+  B_XREAD = B_XFREE + 2,
+  B_PFULL = B_XREAD + 2,
   B_PFREE,
   B_ODONE,
   B_OFREE,
@@ -113,6 +121,20 @@ __device__ inline float4 ld_shared_v4f(uint32_t addr) {
                : "memory");
   return v;
 }
+__device__ inline float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Byte offset of 16-byte chunk c (0..15) of score row h inside one exchange
+// buffer.  Rows h and h^1 interleave at 16 bytes, so the two lanes of a pair
+// fill one 32-byte sector; the chunk order is rotated by the row pair to
+// spread shared-memory banks.
+__device__ inline uint32_t x_off(int h, int c) {
+  const int pr = h >> 1;
+  return (uint32_t)(pr * 512 + ((c ^ (pr & 3)) * 32) + (h & 1) * 16);
+}
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_ckv,
@@ -138,17 +160,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(B_SFULL + i), 1);
-      mbar_init(bar(B_SFREE + i), 128);
+      mbar_init(bar(B_SFREE + i), 256);  // exchange + softmax threads
+      mbar_init(bar(B_XFULL + i), 1);    // local arm + 32 KB of the peer's st.async
+      mbar_init(bar(B_XFREE + i), 1);    // the peer's relay: its buffer is consumed
+      mbar_init(bar(B_XREAD + i), 128);  // local softmax threads consumed buffer i
     }
-    mbar_init(bar(B_XFULL), 128);
-    mbar_init(bar(B_XFREE), 128);
     mbar_init(bar(B_PFULL), 128);
     mbar_init(bar(B_PFREE), 1);
     mbar_init(bar(B_ODONE), 1);
     mbar_init(bar(B_OFREE), 128);
     mbar_init(bar(B_QFULL), 128);
     mbar_init(bar(B_QFREE), 1);
-    mbar_init(bar(B_IDLE), 1);
+    mbar_init(bar(B_IDLE), 2);
+    mbar_expect_tx(bar(B_XFULL), kXBytes);
+    mbar_expect_tx(bar(B_XFULL + 1), kXBytes);
     fence_mbar_init();
     prefetch_tmap(&tm_ckv);
     prefetch_tmap(&tm_kpe);
@@ -178,6 +203,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t tmem = tmem_slot;
   const long long P = sh_P;
   const Walker walker0{sh_b0, sh_s0, range_lo(w, a.G, P), range_lo(w + 1, a.G, P), w, a.G};
+
+  // every lane waits, then the warp agrees, so warp-collective operations never
+  // run with some lanes gone after an aborted wait
+  auto wwait = [&](int i, uint32_t parity) {
+    return __all_sync(0xffffffffu, mbar_wait(bar(i), parity, &abort_flag, a.err));
+  };
+  auto wwait_c = [&](int i, uint32_t parity) {
+    return __all_sync(0xffffffffu, mbar_wait<true>(bar(i), parity, &abort_flag, a.err));
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -212,60 +246,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ S = Q K^T issuer
     if (lane == 0) {
       Walker wk = walker0;
       Unit u;
       uint32_t g = 0, uc = 0;
       bool ok = true;
       const uint32_t idesc_qk = idesc_bf16(128, 64, false, false);
-      const uint32_t idesc_pv = idesc_bf16(128, 256, false, true);
       while (ok && wk.next(a, u)) {
         const int np = u.pe - u.pb;
         if (!mbar_wait(bar(B_QFULL), uc & 1, &abort_flag, a.err)) break;
         tc_fence_after();
-        for (int i = 0; i <= np; ++i) {
-          if (i < np) {  // S = Q K^T for page g+i
-            const uint32_t gi = g + i, s = gi % kStages, sb = gi & 1;
-            if (!mbar_wait(bar(B_FULL + s), (gi / kStages) & 1, &abort_flag, a.err) ||
-                (gi >= 2 && !mbar_wait(bar(B_SFREE + sb), ((gi >> 1) - 1) & 1, &abort_flag, a.err))) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t st = base + s * kStageBytes, d = tmem + kTmS + sb * 64;
-#pragma unroll
-            for (int kk = 0; kk < 16; ++kk)
-              mma_bf16_ts(d, tmem + kTmQ + kk * 8,
-                          sdesc_sw128(st + (kk >> 2) * kBox + (kk & 3) * 32, 16, 1024), idesc_qk,
-                          kk > 0 ? 1u : 0u);
-            if (rank == 1) {
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                mma_bf16_ss(d, sdesc_sw128(base + kOffQpe + kk * 32, 16, 1024),
-                            sdesc_sw128(st + 4 * kBox + kk * 32, 16, 1024), idesc_qk, 1u);
-            }
-            mma_commit(bar(B_SFULL + sb));
-            if (i == np - 1) mma_commit(bar(B_QFREE));
+        for (int i = 0; i < np; ++i) {
+          const uint32_t gi = g + i, s = gi % kStages, sb = gi & 1;
+          if (!mbar_wait(bar(B_FULL + s), (gi / kStages) & 1, &abort_flag, a.err) ||
+              (gi >= 2 && !mbar_wait(bar(B_SFREE + sb), ((gi >> 1) - 1) & 1, &abort_flag, a.err))) {
+            ok = false;
+            break;
           }
-          if (i >= 1) {  // O += P V for page g+i-1
-            const uint32_t gp = g + i - 1, s = gp % kStages;
-            if (!mbar_wait(bar(B_PFULL), gp & 1, &abort_flag, a.err) ||
-                (i == 1 && uc >= 1 && !mbar_wait(bar(B_OFREE), (uc - 1) & 1, &abort_flag, a.err))) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t st = base + s * kStageBytes;
+          tc_fence_after();
+          const uint32_t st = base + s * kStageBytes, d = tmem + kTmS + sb * 64;
+#pragma unroll
+          for (int kk = 0; kk < 16; ++kk)
+            mma_bf16_ts(d, tmem + kTmQ + kk * 8,
+                        sdesc_sw128(st + (kk >> 2) * kBox + (kk & 3) * 32, 16, 1024), idesc_qk,
+                        kk > 0 ? 1u : 0u);
+          if (rank == 1) {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_bf16_ss(tmem + kTmO, sdesc_sw128(base + kOffP + kk * 32, 16, 1024),
-                          sdesc_sw128(st + kk * 2048, kBox, 1024), idesc_pv,
-                          (i > 1 || kk > 0) ? 1u : 0u);
-            mma_commit(bar(B_PFREE));
-            mma_commit(bar(B_EMPTY + s));
-            if (i == np) mma_commit(bar(B_ODONE));
+              mma_bf16_ss(d, sdesc_sw128(base + kOffQpe + kk * 32, 16, 1024),
+                          sdesc_sw128(st + 4 * kBox + kk * 32, 16, 1024), idesc_qk, 1u);
           }
+          mma_commit(bar(B_SFULL + sb));
+          if (i == np - 1) mma_commit(bar(B_QFREE));
         }
         g += np;
         ++uc;
@@ -274,37 +287,108 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       volatile int no_abort = 0;
       mbar_wait(bar(B_IDLE), 0, &no_abort, nullptr);
     }
-  } else if (warp == 3) {
-    // ------------------------------------------------------------ split records
-    if (lane == 0 && rank == 0) {
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ exchange relay
+    if (lane == 0) {
+      const uint32_t xfree_peer0 = mapa(bar(B_XFREE), peer);
       Walker wk = walker0;
       Unit u;
-      int4 first = make_int4(-1, 0, 0, 0), last = make_int4(-1, 0, 0, 0);
-      while (wk.next(a, u)) {
-        const int4 r = make_int4(u.b, u.pb, u.pe, u.split ? 1 : 0);
-        if (u.at_lo) first = r;
-        else if (u.at_hi) last = r;
+      uint32_t g = 0;
+      bool ok = true;
+      while (ok && wk.next(a, u)) {
+        for (int j = u.pb; j < u.pe; ++j, ++g) {
+          const uint32_t sb = g & 1;
+          if (!mbar_wait(bar(B_XREAD + sb), (g >> 1) & 1, &abort_flag, a.err)) { ok = false; break; }
+          mbar_expect_tx(bar(B_XFULL + sb), kXBytes);  // arm for page g+2
+          mbar_arrive_remote(xfree_peer0 + sb * 8);     // the peer may refill it
+        }
       }
-      a.rec[w] = first;
-      a.rec[a.G + w] = last;
     }
-  } else if (warp >= 4) {
-    // ------------------------------------------------------------ softmax warps
+  } else if (warp == 3) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- split records
+      if (rank == 0) {
+        Walker wk = walker0;
+        Unit u;
+        int4 first = make_int4(-1, 0, 0, 0), last = make_int4(-1, 0, 0, 0);
+        while (wk.next(a, u)) {
+          const int4 r = make_int4(u.b, u.pb, u.pe, u.split ? 1 : 0);
+          if (u.at_lo) first = r;
+          else if (u.at_hi) last = r;
+        }
+        a.rec[w] = first;
+        a.rec[a.G + w] = last;
+      }
+      // ---------------------------------------------------------- O += P V issuer
+      Walker wk = walker0;
+      Unit u;
+      uint32_t g = 0, uc = 0;
+      bool ok = true;
+      const uint32_t idesc_pv = idesc_bf16(128, 256, false, true);
+      while (ok && wk.next(a, u)) {
+        const int np = u.pe - u.pb;
+        for (int i = 0; i < np; ++i) {
+          const uint32_t gp = g + i, s = gp % kStages;
+          if (!mbar_wait(bar(B_PFULL), gp & 1, &abort_flag, a.err) ||
+              (i == 0 && uc >= 1 && !mbar_wait(bar(B_OFREE), (uc - 1) & 1, &abort_flag, a.err))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t st = base + s * kStageBytes;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_ss(tmem + kTmO, sdesc_sw128(base + kOffP + kk * 32, 16, 1024),
+                        sdesc_sw128(st + kk * 2048, kBox, 1024), idesc_pv,
+                        (i > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(bar(B_PFREE));
+          mma_commit(bar(B_EMPTY + s));
+          if (i == np - 1) mma_commit(bar(B_ODONE));
+        }
+        g += np;
+        ++uc;
+      }
+      mma_commit(bar(B_IDLE));
+      volatile int no_abort = 0;
+      mbar_wait(bar(B_IDLE), 0, &no_abort, nullptr);
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ------------------------------------------------------------ exchange warps
     const int h = threadIdx.x - 128;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t x_peer = mapa(base + kOffX, peer);
-    const uint32_t xfull_peer = mapa(bar(B_XFULL), peer), xfree_peer = mapa(bar(B_XFREE), peer);
+    const uint32_t xfull_peer0 = mapa(bar(B_XFULL), peer);
+    Walker wk = walker0;
+    Unit u;
+    uint32_t g = 0;
+    bool ok = true;
+    while (ok && wk.next(a, u)) {
+      for (int j = u.pb; j < u.pe; ++j, ++g) {
+        const uint32_t sb = g & 1;
+        if (!wwait(B_SFULL + sb, (g >> 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t s0[32], s1[32];
+        tmem_ld32(tmem + lane_base + kTmS + sb * 64, s0);
+        tmem_ld32(tmem + lane_base + kTmS + sb * 64 + 32, s1);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(bar(B_SFREE + sb));
+        // the peer's buffer sb is free once it has consumed page g-2
+        if (g >= 2 && !wwait_c(B_XFREE + sb, ((g >> 1) - 1) & 1)) { ok = false; break; }
+        const uint32_t dst = x_peer + sb * kXBytes, xb = xfull_peer0 + sb * 8;
+#pragma unroll
+        for (int cc = 0; cc < 16; ++cc) {
+          const uint32_t* v = cc < 8 ? &s0[cc * 4] : &s1[(cc - 8) * 4];
+          st_async_v4(dst + x_off(h, cc), v[0], v[1], v[2], v[3], xb);
+        }
+      }
+    }
+  } else if (warp >= 8) {
+    // ------------------------------------------------------------ softmax warps
+    const int h = threadIdx.x - 256;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const float c = a.scale_log2;
     const int H = a.H;
-
-    // every lane waits, then the warp agrees, so warp-collective operations
-    // never run with some lanes gone after an aborted wait
-    auto wwait = [&](int i, uint32_t parity) {
-      return __all_sync(0xffffffffu, mbar_wait(bar(i), parity, &abort_flag, a.err));
-    };
-    auto wwait_c = [&](int i, uint32_t parity) {
-      return __all_sync(0xffffffffu, mbar_wait<true>(bar(i), parity, &abort_flag, a.err));
-    };
 
     auto load_q = [&](const Unit& q) {
       // query latent half -> tensor memory (two bf16 per column); q_pe -> smem
@@ -350,11 +434,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int j = u.pb + i;
         const int page = a.page_table[(size_t)u.b * a.maxp + j];
         const bool page_ok = page >= 0 && page < a.num_pages;
-        if (!page_ok && h == 0 && rank == 0) set_error(a.err, MLA_ERR_PAGE_OOB);
         const int valid = page_ok ? min(kPage, u.n - j * kPage) : 0;
+        if (!page_ok && h == 0 && rank == 0) set_error(a.err, MLA_ERR_PAGE_OOB);
 
-        // my partial scores
-        if (!wwait(B_SFULL + sb, (gi >> 1) & 1)) { ok = false; break; }
+        // own partial scores, plus the peer's from the exchange buffer
+        if (!wwait_c(B_XFULL + sb, (gi >> 1) & 1) || !wwait(B_SFULL + sb, (gi >> 1) & 1)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         uint32_t s0[32], s1[32];
         tmem_ld32(tmem + lane_base + kTmS + sb * 64, s0);
@@ -362,53 +449,49 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(bar(B_SFREE + sb));
-
-        // swap partial scores with the peer CTA
-        if (gi >= 1 && !wwait_c(B_XFREE, (gi - 1) & 1)) { ok = false; break; }
-        const uint32_t xrow = h * 256;
-#pragma unroll
-        for (int cc = 0; cc < 16; ++cc) {
-          const uint32_t* src = cc < 8 ? &s0[cc * 4] : &s1[(cc - 8) * 4];
-          st_cluster_v4(x_peer + xrow + ((cc ^ (h & 15)) * 16), src[0], src[1], src[2], src[3]);
-        }
-        mbar_arrive_remote(xfull_peer);
-        if (!wwait_c(B_XFULL, gi & 1)) { ok = false; break; }
         float x[64];
+        const uint32_t xb = base + kOffX + sb * kXBytes;
 #pragma unroll
         for (int cc = 0; cc < 16; ++cc) {
-          const float4 v = ld_shared_v4f(base + kOffX + xrow + ((cc ^ (h & 15)) * 16));
+          const float4 v = ld_shared_v4f(xb + x_off(h, cc));
           const uint32_t* own = cc < 8 ? &s0[cc * 4] : &s1[(cc - 8) * 4];
           x[cc * 4 + 0] = __uint_as_float(own[0]) + v.x;
           x[cc * 4 + 1] = __uint_as_float(own[1]) + v.y;
           x[cc * 4 + 2] = __uint_as_float(own[2]) + v.z;
           x[cc * 4 + 3] = __uint_as_float(own[3]) + v.w;
         }
-        mbar_arrive_remote(xfree_peer);
+        mbar_arrive(bar(B_XREAD + sb));  // relayed to the peer by warp 2
 
-        // online softmax in the log2 domain, lazy rescaling
-        float mx = -INFINITY;
+        // online softmax in the log2 domain with lazy rescaling
+        if (valid < kPage) {
 #pragma unroll
-        for (int k = 0; k < 64; ++k) {
-          x[k] = k < valid ? x[k] * c : -INFINITY;
-          mx = fmaxf(mx, x[k]);
+          for (int k = 0; k < 64; ++k) x[k] = k < valid ? x[k] : -INFINITY;
         }
+        float t[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) t[k] = fmaxf(fmaxf(x[k], x[k + 16]), fmaxf(x[k + 32], x[k + 48]));
+#pragma unroll
+        for (int k = 0; k < 8; ++k) t[k] = fmaxf(t[k], t[k + 8]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) t[k] = fmaxf(t[k], t[k + 4]);
+        const float mx = fmaxf(fmaxf(t[0], t[1]), fmaxf(t[2], t[3])) * c;
         float alpha = 1.f;
         bool resc = false;
         if (mx > m + kRescaleLog2) {
-          alpha = exp2f(m - mx);
+          alpha = ex2(m - mx);
           resc = i > 0;
           m = mx;
         }
         const float mm = m == -INFINITY ? 0.f : m;
-        float sum = 0.f;
+        float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         uint32_t pk[32];
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
-          const float p0 = exp2f(x[2 * k] - mm), p1 = exp2f(x[2 * k + 1] - mm);
-          sum += p0 + p1;
+          const float p0 = ex2(fmaf(x[2 * k], c, -mm)), p1 = ex2(fmaf(x[2 * k + 1], c, -mm));
+          ps[k & 7] += p0 + p1;
           pk[k] = pack_bf16(p0, p1);
         }
-        l = l * alpha + sum;
+        l = l * alpha + (((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7])));
 
         // zero cache rows past the sequence end (garbage could be NaN)
         if (valid < kPage) {

@@ -240,6 +240,16 @@ __device__ inline void st_cluster_v4(uint32_t caddr, uint32_t a, uint32_t b, uin
                "r"(d)
                : "memory");
 }
+// Asynchronous 16-byte store into another CTA's shared memory; completes
+// 16 bytes of transaction count on that CTA's mbarrier (both addresses from
+// mapa).  No fence is needed: the receiver's wait on the mbarrier observes it.
+__device__ inline void st_async_v4(uint32_t caddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                   uint32_t cbar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1,%2,%3,%4}, [%5];" ::"r"(caddr),
+      "r"(a), "r"(b), "r"(c), "r"(d), "r"(cbar)
+      : "memory");
+}
 // Arrive on a barrier given by its shared::cluster address (from mapa).
 __device__ inline void mbar_arrive_remote(uint32_t caddr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr)
