@@ -212,6 +212,35 @@ mla_status mla_cache_append(const mla_params* p, const void* kv_rows, const int3
 mla_status mla_rope_q(const mla_params* p, const void* q_pe_raw, const int32_t* seq_lens,
                       void* q_pe, mla_stream_t stream);
 
+/* ---------------------------------------------------------------------
+ * mla_decode_static: mla_decode followed by mla_split_kv_combine, for
+ * callers that cannot allocate device memory.  The pages have no counterpart:
+ * this is a calling convention, not a step of the method.
+ * Some callers are handed their input and output buffers but may not create
+ * any of their own: a plugin inside a host application or serving runtime
+ * that has reserved all device memory in its own pool, or a latency-critical
+ * path where cudaMalloc (which can synchronise the device) is not allowed.
+ * This entry point needs no workspace argument: its scratch is a fixed
+ * 32 MiB array inside the library's device image, which every GPU that
+ * loads the library keeps until the process exits.  It allocates nothing
+ * and calls no allocating routine.
+ *   Arguments: as mla_decode, without num_splits and the workspace; the KV
+ *   partition count is the automatic one, lowered until the scratch fits.
+ *   Returns MLA_ERR_WORKSPACE when even one partition does not fit (very
+ *   large B*H); other host-side errors as mla_decode.
+ *   Device-side input faults (bad page ids or lengths) are handled as in
+ *   mla_decode but are not reported: the error word is in the shared array.
+ * The first call on a device looks up the array's device address for that
+ * device (once, with the device current); make that first call before any
+ * stream capture.  All calls share the one array, and each call keeps the
+ * previous call's contents until it overwrites them: calls that overlap on
+ * the GPU (other streams, other threads) race and must be serialised by the
+ * caller. */
+mla_status mla_decode_static(const mla_params* p, const void* q_lat, const void* q_pe,
+                             const void* ckv_cache, const void* kpe_cache, const float* kv_scale,
+                             const int32_t* page_table, const int32_t* seq_lens, void* o_lat,
+                             float* lse, mla_stream_t stream);
+
 /* mla_workspace_status: copy the workspace's sticky error word to the host
  * (synchronises `stream`) and return it as a status; clear it when `clear`
  * is non-zero. */

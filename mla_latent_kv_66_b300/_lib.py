@@ -61,6 +61,7 @@ _SIGS = {
                                         _P, _P, _P, _P]),
     "mla_rope_q": (ctypes.c_int, [ctypes.POINTER(MlaParams), _P, _P, _P, _P]),
     "mla_workspace_status": (ctypes.c_int, [_P, ctypes.c_int, _P]),
+    "mla_decode_static": (ctypes.c_int, [ctypes.POINTER(MlaParams), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
 }
 
 
@@ -154,3 +155,11 @@ def mla_rope_q(p, q_pe_raw, seq_lens, q_pe, stream=None):
 
 def mla_workspace_status(workspace, clear=False, stream=None) -> int:
     return lib.mla_workspace_status(_ptr(workspace), 1 if clear else 0, _stream(stream))
+
+
+def mla_decode_static(p, q_lat, q_pe, ckv, kpe, kv_scale, page_table, seq_lens, o_lat, lse=None, stream=None):
+    """Decode + split-KV combine with the library's fixed internal scratch
+    (for callers that may not allocate device memory)."""
+    _check(lib.mla_decode_static(ctypes.byref(p), _ptr(q_lat), _ptr(q_pe), _ptr(ckv), _ptr(kpe), _ptr(kv_scale),
+                                 _ptr(page_table), _ptr(seq_lens), _ptr(o_lat), _ptr(lse), _stream(stream)),
+           "mla_decode_static")
