@@ -11,25 +11,33 @@
 //   rank 0: latent columns [0,256);  rank 1: latent [256,512) and k_pe.
 // Each CTA TMA-loads only its part of every page and computes the partial
 // score over its part (rank 1 adds the shared RoPE key).  The two partial
-// score tiles are swapped through distributed shared memory and added in
-// both CTAs (fp32 addition commutes, so both see the same scores and make
-// the same softmax decisions); each CTA then accumulates P . c over its own
-// 256 latent columns.
+// score tiles are swapped through distributed shared memory in the log2
+// domain as fp16 (half the bytes of fp32; the SM-to-SM network, not HBM, is
+// the scarce resource here) and each CTA adds its own fp32 partial to the
+// peer's fp16 one.  The two CTAs' scores therefore differ by the fp16
+// rounding of one partial (2^-11 relative), so each CTA normalises its half
+// of O with its own row sum; rank 0's log-sum-exp is the one reported.  Each
+// CTA then accumulates P . c over its own 256 latent columns.
 //
-// Warp roles (384 threads):
-//   warp 0       TMA producer (cache pages, 3-stage ring)
+// Warp roles (512 threads):
+//   warp 0       TMA producer (cache pages, 3-stage ring, L2 prefetch ahead)
 //   warp 1       MMA issuer for S = Q K^T (A = query in tensor memory)
 //   warp 2       tensor-memory allocation; then relays "exchange buffer
 //                consumed" to the peer CTA and re-arms the receive barrier
 //   warp 3       KV-partition schedule, split records; then MMA issuer for
 //                O += P V (a separate issuer lets S = Q K^T run ahead)
-//   warps 4..7   exchange: push each partial score tile to the peer CTA with
-//                asynchronous remote stores (st.async) as soon as its
-//                S = Q K^T completes; double-buffered
-//   warps 8..11  softmax: thread = head row; add the peer's partial, online
-//                softmax with lazy rescaling, P to shared memory, O rescale,
-//                per-unit epilogue
+//   warps 4..7   exchange: stage each partial score tile (fp16) in shared
+//                memory as soon as its S = Q K^T completes and send it to the
+//                peer CTA with one bulk copy; double-buffered
+//   warps 8..15  two softmax warpgroups; warpgroup j owns tokens [32j, 32j+32)
+//                of every page, thread = head row: own fp32 partial + the
+//                peer's fp16 partial, row maximum agreed with the other
+//                warpgroup, online softmax with lazy rescaling, its half of P
+//                to shared memory, its half of O rescaled when needed and
+//                written at the end of a unit.
 // Tensor memory: O [0,256), S double buffer [256,384), query [384,512).
+#include <cuda_fp16.h>
+
 #include "kernels.h"
 #include "tc.cuh"
 #include "tmap.cuh"
@@ -44,12 +52,14 @@ constexpr uint32_t kBox = 8192;             // [64 rows x 64 bf16], 128-byte swi
 constexpr uint32_t kStageBytes = 5 * kBox;  // 4 latent boxes + k_pe box (rank 1)
 constexpr uint32_t kOffQpe = kStages * kStageBytes;  // [128 x 64] bf16 (rank 1)
 constexpr uint32_t kOffP = kOffQpe + 16384;          // [128 x 64] bf16 probabilities
-constexpr uint32_t kOffX = kOffP + 16384;            // 2 x [128 x 64] fp32 peer partial scores
-constexpr uint32_t kXBytes = 32768;
-constexpr uint32_t kSmemBytes = kOffX + 2 * kXBytes + 1024;
+constexpr uint32_t kOffX = kOffP + 16384;            // 2 x [128 x 64] fp16 peer partial scores
+constexpr uint32_t kXBytes = 16384;
+constexpr uint32_t kOffXs = kOffX + 2 * kXBytes;     // 2 x [128 x 64] fp16 own partial, outgoing
+constexpr uint32_t kSmemBytes = kOffXs + 2 * kXBytes + 1024;
 constexpr uint32_t kTmO = 0, kTmS = 256, kTmQ = 384;
-constexpr int kThreads = 384;
+constexpr int kThreads = 512;
 constexpr float kRescaleLog2 = 8.f;  // lazy rescale threshold: P stays <= 2^8
+constexpr int kPrefetchPages = 6;    // L2 prefetch distance of the producer, in pages
 
 enum {
   B_FULL = 0,
@@ -66,7 +76,9 @@ enum {
   B_QFULL,
   B_QFREE,
   B_IDLE,
-  B_COUNT
+  B_MX,
+  B_XSTAGED,
+  B_COUNT = B_XSTAGED + 2
 };
 
 struct Unit {
@@ -113,10 +125,10 @@ __device__ inline void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint3
   asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
                : "memory");
 }
-__device__ inline float4 ld_shared_v4f(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+__device__ inline uint4 ld_shared_v4u(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "r"(addr)
                : "memory");
   return v;
@@ -127,13 +139,18 @@ __device__ inline float ex2(float x) {
   return y;
 }
 
-// Byte offset of 16-byte chunk c (0..15) of score row h inside one exchange
-// buffer.  Rows h and h^1 interleave at 16 bytes, so the two lanes of a pair
-// fill one 32-byte sector; the chunk order is rotated by the row pair to
-// spread shared-memory banks.
-__device__ inline uint32_t x_off(int h, int c) {
-  const int pr = h >> 1;
-  return (uint32_t)(pr * 512 + ((c ^ (pr & 3)) * 32) + (h & 1) * 16);
+// Byte offset of 16-byte chunk c (0..7) of score row h inside one exchange
+// buffer: a row is 64 fp16 values (128 bytes); the chunk order is rotated by
+// the row so that 8 consecutive rows touch 8 different bank groups.
+__device__ inline uint32_t x_off(int h, int c) { return (uint32_t)(h * 128 + ((c ^ (h & 7)) * 16)); }
+
+// Two fp32 values as one packed fp16 pair (round to nearest even), and back.
+__device__ inline uint32_t pack_h2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ inline float2 unpack_h2(uint32_t u) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&u));
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -145,6 +162,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   __shared__ int abort_flag;
   __shared__ long long sh_P, sh_s0;
   __shared__ int sh_b0;
+  __shared__ uint16_t mx_swap[2][2][128];  // row maxima between the two softmax warpgroups
 
   const uint32_t rank = cluster_rank(), peer = rank ^ 1u;
   const int w = blockIdx.x >> 1;
@@ -160,18 +178,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(B_SFULL + i), 1);
-      mbar_init(bar(B_SFREE + i), 256);  // exchange + softmax threads
-      mbar_init(bar(B_XFULL + i), 1);    // local arm + 32 KB of the peer's st.async
+      mbar_init(bar(B_SFREE + i), 384);  // exchange + both softmax warpgroups
+      mbar_init(bar(B_XFULL + i), 1);    // local arm + 16 KB of the peer's st.async
       mbar_init(bar(B_XFREE + i), 1);    // the peer's relay: its buffer is consumed
-      mbar_init(bar(B_XREAD + i), 128);  // local softmax threads consumed buffer i
+      mbar_init(bar(B_XREAD + i), 256);  // local softmax threads consumed buffer i
     }
-    mbar_init(bar(B_PFULL), 128);
+    mbar_init(bar(B_PFULL), 256);
     mbar_init(bar(B_PFREE), 1);
     mbar_init(bar(B_ODONE), 1);
-    mbar_init(bar(B_OFREE), 128);
-    mbar_init(bar(B_QFULL), 128);
+    mbar_init(bar(B_OFREE), 256);
+    mbar_init(bar(B_QFULL), 256);
     mbar_init(bar(B_QFREE), 1);
     mbar_init(bar(B_IDLE), 2);
+    mbar_init(bar(B_MX), 256);
+    mbar_init(bar(B_XSTAGED), 128);
+    mbar_init(bar(B_XSTAGED + 1), 128);
     mbar_expect_tx(bar(B_XFULL), kXBytes);
     mbar_expect_tx(bar(B_XFULL + 1), kXBytes);
     fence_mbar_init();
@@ -216,11 +237,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      Walker wk = walker0;
-      Unit u;
+      Walker wk = walker0, pf = walker0;
+      Unit u, pu;
       uint32_t g = 0;
       bool ok = true;
       const uint32_t tx = rank == 0 ? 4 * kBox : 5 * kBox;
+      // L2 prefetch runs kPrefetchPages pages ahead of the TMA ring, so the
+      // ring's loads hit L2; rank 0 fetches the whole latent page, rank 1
+      // the rope page.
+      bool pf_have = pf.next(a, pu);
+      int pj = pf_have ? pu.pb : 0;
+      auto prefetch_next = [&]() {
+        if (!pf_have) return;
+        const int page = a.page_table[(size_t)pu.b * a.maxp + pj];
+        if (page >= 0 && page < a.num_pages) {
+          if (rank == 0)
+            prefetch_l2(static_cast<const uint8_t*>(a.ckv) + (size_t)page * kPage * kLatent * 2,
+                        kPage * kLatent * 2);
+          else
+            prefetch_l2(static_cast<const uint8_t*>(a.kpe) + (size_t)page * kPage * kRope * 2,
+                        kPage * kRope * 2);
+        }
+        if (++pj >= pu.pe) {
+          pf_have = pf.next(a, pu);
+          pj = pf_have ? pu.pb : 0;
+        }
+      };
+      for (int i = 0; i < kPrefetchPages; ++i) prefetch_next();
       while (ok && wk.next(a, u)) {
         for (int j = u.pb; j < u.pe; ++j, ++g) {
           const uint32_t s = g % kStages;
@@ -237,6 +280,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 4; ++i)
             tma_load_2d(st + i * kBox, &tm_ckv, bar(B_FULL + s), (int)rank * 256 + i * 64, page * kPage);
           if (rank == 1) tma_load_2d(st + 4 * kBox, &tm_kpe, bar(B_FULL + s), 0, page * kPage);
+          prefetch_next();
         }
       }
       // copies still in flight must land before the CTA can exit
@@ -352,49 +396,101 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       volatile int no_abort = 0;
       mbar_wait(bar(B_IDLE), 0, &no_abort, nullptr);
     }
-  } else if (warp >= 4 && warp < 8) {
+  } else if (warp < 8) {
     // ------------------------------------------------------------ exchange warps
+    // Stage each page's partial score (log2 domain, fp16) in shared memory as
+    // soon as its S = Q K^T completes; one thread then hands the 16 KB to the
+    // async copy engine, which writes it into the peer CTA and completes the
+    // peer's receive barrier.  (Per-thread remote stores would queue behind
+    // the SM-to-SM network and hold up the softmax warps' shared-memory
+    // traffic.)
     const int h = threadIdx.x - 128;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t x_peer = mapa(base + kOffX, peer);
     const uint32_t xfull_peer0 = mapa(bar(B_XFULL), peer);
+    const float c = a.scale_log2;
     Walker wk = walker0;
     Unit u;
     uint32_t g = 0;
     bool ok = true;
     while (ok && wk.next(a, u)) {
-      for (int j = u.pb; j < u.pe; ++j, ++g) {
+      for (int jp = u.pb; jp < u.pe; ++jp, ++g) {
         const uint32_t sb = g & 1;
         if (!wwait(B_SFULL + sb, (g >> 1) & 1)) { ok = false; break; }
         tc_fence_after();
-        uint32_t s0[32], s1[32];
-        tmem_ld32(tmem + lane_base + kTmS + sb * 64, s0);
-        tmem_ld32(tmem + lane_base + kTmS + sb * 64 + 32, s1);
-        tmem_wait_ld();
+        uint32_t hx[32];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t s32[32];
+          tmem_ld32(tmem + lane_base + kTmS + sb * 64 + half * 32, s32);
+          tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 16; ++k)
+            hx[half * 16 + k] = pack_h2(__uint_as_float(s32[2 * k]) * c, __uint_as_float(s32[2 * k + 1]) * c);
+        }
         tc_fence_before();
         mbar_arrive(bar(B_SFREE + sb));
-        // the peer's buffer sb is free once it has consumed page g-2
+        // staging buffer sb and the peer's buffer sb are free once the peer has
+        // consumed page g-2 (its copy has then finished reading ours)
         if (g >= 2 && !wwait_c(B_XFREE + sb, ((g >> 1) - 1) & 1)) { ok = false; break; }
-        const uint32_t dst = x_peer + sb * kXBytes, xb = xfull_peer0 + sb * 8;
+        const uint32_t stg = base + kOffXs + sb * kXBytes;
 #pragma unroll
-        for (int cc = 0; cc < 16; ++cc) {
-          const uint32_t* v = cc < 8 ? &s0[cc * 4] : &s1[(cc - 8) * 4];
-          st_async_v4(dst + x_off(h, cc), v[0], v[1], v[2], v[3], xb);
+        for (int cc = 0; cc < 8; ++cc)
+          st_shared_v4(stg + x_off(h, cc), hx[4 * cc], hx[4 * cc + 1], hx[4 * cc + 2], hx[4 * cc + 3]);
+        fence_proxy_async_smem();
+        mbar_arrive(bar(B_XSTAGED + sb));
+        if (h == 0) {
+          if (!mbar_wait(bar(B_XSTAGED + sb), (g >> 1) & 1, &abort_flag, a.err)) { ok = false; }
+          else bulk_copy_to_peer(x_peer + sb * kXBytes, stg, kXBytes, xfull_peer0 + sb * 8);
         }
+        if (!__all_sync(0xffffffffu, ok)) break;
       }
     }
-  } else if (warp >= 8) {
-    // ------------------------------------------------------------ softmax warps
-    const int h = threadIdx.x - 256;
+  } else {
+    // ------------------------------------------------------------ softmax warpgroups
+    // Warpgroup j (warps 8+4j .. 11+4j) owns score columns [32j, 32j+32) of
+    // every page (its 32 tokens) for all 128 head rows; thread = head row =
+    // tensor-memory lane.  It adds its own fp32 partial score to the peer's
+    // fp16 one and agrees on the row maximum with the other warpgroup.
+    const int j = (warp - 8) >> 2;
+    const int h = (warp & 3) * 32 + lane;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const float c = a.scale_log2;
     const int H = a.H;
+    // the P buffer doubles as the exchange area of the row sums at the end of a
+    // unit, when no P . V is pending
+    uint32_t* const lsum_swap = reinterpret_cast<uint32_t*>(smem_raw + (base + kOffP - smem_u32(smem_raw)));
+    uint32_t xk = 0;  // phases of the warpgroup-exchange barrier consumed
+
+    // Swap one value per row with the other warpgroup (bounded wait).  Row
+    // maxima travel as fp16 bit patterns and alternate between two slots, so
+    // that a fast warpgroup cannot overwrite a value the other has not read
+    // yet.
+    auto swap_max = [&](uint32_t mine, uint32_t& other) -> bool {
+      const uint32_t slot = xk & 1;
+      mx_swap[slot][j][h] = (uint16_t)mine;
+      mbar_arrive(bar(B_MX));
+      const bool okw = wwait(B_MX, xk & 1);
+      ++xk;
+      other = mx_swap[slot][j ^ 1][h];
+      return okw;
+    };
+    auto swap_sum = [&](uint32_t mine, uint32_t& other) -> bool {
+      lsum_swap[j * 128 + h] = mine;
+      mbar_arrive(bar(B_MX));
+      const bool okw = wwait(B_MX, xk & 1);
+      ++xk;
+      other = lsum_swap[(j ^ 1) * 128 + h];
+      return okw;
+    };
 
     auto load_q = [&](const Unit& q) {
-      // query latent half -> tensor memory (two bf16 per column); q_pe -> smem
-      const uint4* src = reinterpret_cast<const uint4*>(a.q_lat + ((size_t)q.b * H + h) * kLatent + rank * 256);
+      // this warpgroup's 128 latent values of the query half -> tensor memory
+      // columns [64j, 64j+64) (two bf16 per column); q_pe -> shared memory
+      const uint4* src = reinterpret_cast<const uint4*>(
+          a.q_lat + ((size_t)q.b * H + h) * kLatent + rank * 256 + j * 128);
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int cc = 0; cc < 2; ++cc) {
         uint32_t r[32];
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
@@ -404,9 +500,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           r[4 * v + 2] = x.z;
           r[4 * v + 3] = x.w;
         }
-        tmem_st32(tmem + lane_base + kTmQ + cc * 32, r);
+        tmem_st32(tmem + lane_base + kTmQ + j * 64 + cc * 32, r);
       }
-      if (rank == 1) {
+      if (rank == 1 && j == 0) {
         const uint4* sp = reinterpret_cast<const uint4*>(a.q_pe + ((size_t)q.b * H + h) * kRope);
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc) {
@@ -431,50 +527,55 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       float m = -INFINITY, l = 0.f;
       for (int i = 0; i < np; ++i) {
         const uint32_t gi = g + i, sb = gi & 1, s = gi % kStages;
-        const int j = u.pb + i;
-        const int page = a.page_table[(size_t)u.b * a.maxp + j];
+        const int jp = u.pb + i;
+        const int page = a.page_table[(size_t)u.b * a.maxp + jp];
         const bool page_ok = page >= 0 && page < a.num_pages;
-        const int valid = page_ok ? min(kPage, u.n - j * kPage) : 0;
-        if (!page_ok && h == 0 && rank == 0) set_error(a.err, MLA_ERR_PAGE_OOB);
+        const int valid = page_ok ? min(kPage, u.n - jp * kPage) : 0;
+        if (!page_ok && h == 0 && j == 0 && rank == 0) set_error(a.err, MLA_ERR_PAGE_OOB);
 
-        // own partial scores, plus the peer's from the exchange buffer
-        if (!wwait_c(B_XFULL + sb, (gi >> 1) & 1) || !wwait(B_SFULL + sb, (gi >> 1) & 1)) {
-          ok = false;
-          break;
-        }
+        // own partial score (fp32) plus the peer's (fp16), in the log2 domain
+        if (!wwait(B_SFULL + sb, (gi >> 1) & 1)) { ok = false; break; }
         tc_fence_after();
-        uint32_t s0[32], s1[32];
-        tmem_ld32(tmem + lane_base + kTmS + sb * 64, s0);
-        tmem_ld32(tmem + lane_base + kTmS + sb * 64 + 32, s1);
+        uint32_t s32[32];
+        tmem_ld32(tmem + lane_base + kTmS + sb * 64 + j * 32, s32);
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(bar(B_SFREE + sb));
-        float x[64];
-        const uint32_t xb = base + kOffX + sb * kXBytes;
+        if (!wwait_c(B_XFULL + sb, (gi >> 1) & 1)) { ok = false; break; }
+        float x[32];
+        const uint32_t xbuf = base + kOffX + sb * kXBytes;
 #pragma unroll
-        for (int cc = 0; cc < 16; ++cc) {
-          const float4 v = ld_shared_v4f(xb + x_off(h, cc));
-          const uint32_t* own = cc < 8 ? &s0[cc * 4] : &s1[(cc - 8) * 4];
-          x[cc * 4 + 0] = __uint_as_float(own[0]) + v.x;
-          x[cc * 4 + 1] = __uint_as_float(own[1]) + v.y;
-          x[cc * 4 + 2] = __uint_as_float(own[2]) + v.z;
-          x[cc * 4 + 3] = __uint_as_float(own[3]) + v.w;
+        for (int cc = 0; cc < 4; ++cc) {
+          const uint4 v = ld_shared_v4u(xbuf + x_off(h, 4 * j + cc));
+          const uint32_t pv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 b2 = unpack_h2(pv[e]);
+            const int k = 8 * cc + 2 * e;
+            x[k] = fmaf(__uint_as_float(s32[k]), c, b2.x);
+            x[k + 1] = fmaf(__uint_as_float(s32[k + 1]), c, b2.y);
+          }
         }
         mbar_arrive(bar(B_XREAD + sb));  // relayed to the peer by warp 2
-
-        // online softmax in the log2 domain with lazy rescaling
-        if (valid < kPage) {
+        if (valid < kPage) {  // tokens past the sequence end (or a bad page)
 #pragma unroll
-          for (int k = 0; k < 64; ++k) x[k] = k < valid ? x[k] : -INFINITY;
+          for (int k = 0; k < 32; ++k) x[k] = 32 * j + k < valid ? x[k] : -INFINITY;
         }
-        float t[16];
+        float t8[8];
 #pragma unroll
-        for (int k = 0; k < 16; ++k) t[k] = fmaxf(fmaxf(x[k], x[k + 16]), fmaxf(x[k + 32], x[k + 48]));
+        for (int k = 0; k < 8; ++k) t8[k] = fmaxf(fmaxf(x[k], x[k + 8]), fmaxf(x[k + 16], x[k + 24]));
 #pragma unroll
-        for (int k = 0; k < 8; ++k) t[k] = fmaxf(t[k], t[k + 8]);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) t[k] = fmaxf(t[k], t[k + 4]);
-        const float mx = fmaxf(fmaxf(t[0], t[1]), fmaxf(t[2], t[3])) * c;
+        for (int k = 0; k < 4; ++k) t8[k] = fmaxf(t8[k], t8[k + 4]);
+        // the row maximum is swapped rounded up to fp16: an upper bound that
+        // both warpgroups share exactly
+        const uint32_t mine = __half_as_ushort(__float2half_ru(fmaxf(fmaxf(t8[0], t8[1]), fmaxf(t8[2], t8[3]))));
+        uint32_t other;
+        if (!swap_max(mine, other)) { ok = false; break; }
+        const float mx = fmaxf(__half2float(__ushort_as_half((unsigned short)mine)),
+                               __half2float(__ushort_as_half((unsigned short)other)));
+
+        // online softmax with lazy rescaling: both warpgroups hold the same m
+        // and take the same decisions
         float alpha = 1.f;
         bool resc = false;
         if (mx > m + kRescaleLog2) {
@@ -483,21 +584,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           m = mx;
         }
         const float mm = m == -INFINITY ? 0.f : m;
-        float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        uint32_t pk[32];
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t pk[16];
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const float p0 = ex2(fmaf(x[2 * k], c, -mm)), p1 = ex2(fmaf(x[2 * k + 1], c, -mm));
-          ps[k & 7] += p0 + p1;
+        for (int k = 0; k < 16; ++k) {
+          const float p0 = ex2(x[2 * k] - mm), p1 = ex2(x[2 * k + 1] - mm);
+          ps[k & 3] += p0 + p1;
           pk[k] = pack_bf16(p0, p1);
         }
-        l = l * alpha + (((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7])));
+        l = l * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
 
         // zero cache rows past the sequence end (garbage could be NaN)
         if (valid < kPage) {
           const uint32_t st = base + s * kStageBytes;
           const int rows = kPage - valid, per_box = rows * 8;
-          for (int idx = h; idx < 4 * per_box; idx += 128) {
+          for (int idx = h + 128 * j; idx < 4 * per_box; idx += 256) {
             const int box = idx / per_box, rem = idx % per_box;
             st_shared_v4(st + box * kBox + (valid + rem / 8) * 128 + (rem % 8) * 16, 0, 0, 0, 0);
           }
@@ -506,23 +607,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // P buffer and O are free once the previous page's P V has finished
         if (gi >= 1 && !wwait(B_PFREE, (gi - 1) & 1)) { ok = false; break; }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, resc)) {
+        if (__any_sync(0xffffffffu, resc)) {  // this warpgroup's 128 O columns
           const float f = resc ? alpha : 1.f;
 #pragma unroll 1
-          for (int cc = 0; cc < 8; ++cc) {
+          for (int cc = 0; cc < 4; ++cc) {
             uint32_t r[32];
-            tmem_ld32(tmem + lane_base + kTmO + cc * 32, r);
+            const uint32_t col = tmem + lane_base + kTmO + j * 128 + cc * 32;
+            tmem_ld32(col, r);
             tmem_wait_ld();
 #pragma unroll
             for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * f);
-            tmem_st32(tmem + lane_base + kTmO + cc * 32, r);
+            tmem_st32(col, r);
           }
           tmem_wait_st();
         }
 #pragma unroll
-        for (int cc = 0; cc < 8; ++cc)
-          st_shared_v4(base + kOffP + h * 128 + ((cc ^ (h & 7)) * 16), pk[4 * cc], pk[4 * cc + 1],
-                       pk[4 * cc + 2], pk[4 * cc + 3]);
+        for (int cc = 0; cc < 4; ++cc)
+          st_shared_v4(base + kOffP + h * 128 + (((4 * j + cc) ^ (h & 7)) * 16), pk[4 * cc],
+                       pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(bar(B_PFULL));
@@ -538,20 +640,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         load_q(nu);
       }
 
-      // epilogue: normalise this CTA's 256 latent columns of every head row
+      // epilogue: the row sum is the two warpgroups' partial sums; each
+      // normalises its 128 of this CTA's 256 latent columns
       if (!wwait(B_ODONE, uc & 1)) break;
       tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      uint32_t l_other;
+      if (!swap_sum(__float_as_uint(l), l_other)) break;
+      const float lt = l + __uint_as_float(l_other);
+      const float inv = lt > 0.f ? 1.f / lt : 0.f;
       const size_t row = (size_t)u.b * H + h;
       const size_t prow = (size_t)u.slot * H + h;
+      const int col0 = rank * 256 + j * 128;
 #pragma unroll 1
-      for (int cc = 0; cc < 8; ++cc) {
+      for (int cc = 0; cc < 4; ++cc) {
         uint32_t r[32];
-        tmem_ld32(tmem + lane_base + kTmO + cc * 32, r);
+        tmem_ld32(tmem + lane_base + kTmO + j * 128 + cc * 32, r);
         tmem_wait_ld();
         if (h < H) {
           if (!u.split) {
-            uint4* dst = reinterpret_cast<uint4*>(a.o_lat + row * kLatent + rank * 256 + cc * 32);
+            uint4* dst = reinterpret_cast<uint4*>(a.o_lat + row * kLatent + col0 + cc * 32);
 #pragma unroll
             for (int v = 0; v < 4; ++v)
               dst[v] = make_uint4(pack_bf16(__uint_as_float(r[8 * v]) * inv, __uint_as_float(r[8 * v + 1]) * inv),
@@ -559,7 +666,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                   pack_bf16(__uint_as_float(r[8 * v + 4]) * inv, __uint_as_float(r[8 * v + 5]) * inv),
                                   pack_bf16(__uint_as_float(r[8 * v + 6]) * inv, __uint_as_float(r[8 * v + 7]) * inv));
           } else {
-            float4* dst = reinterpret_cast<float4*>(a.part_o + prow * kLatent + rank * 256 + cc * 32);
+            float4* dst = reinterpret_cast<float4*>(a.part_o + prow * kLatent + col0 + cc * 32);
 #pragma unroll
             for (int v = 0; v < 8; ++v)
               dst[v] = make_float4(__uint_as_float(r[4 * v]) * inv, __uint_as_float(r[4 * v + 1]) * inv,
@@ -567,8 +674,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (rank == 0 && h < H) {
-        const float lse = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+      if (rank == 0 && j == 0 && h < H) {
+        const float lse = lt > 0.f ? (m + log2f(lt)) * kLn2 : -INFINITY;
         if (!u.split) {
           if (a.lse) a.lse[row] = lse;
         } else {
@@ -583,7 +690,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       have = have_next;
     }
   }
-
   tc_fence_before();
   __syncthreads();
   cluster_sync();  // the peer no longer touches this CTA's shared memory

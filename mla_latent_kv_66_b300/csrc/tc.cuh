@@ -114,6 +114,14 @@ __device__ inline void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_
       : "memory");
 }
 
+// Bring `bytes` (multiple of 16, 16-byte aligned address) of global memory
+// into L2 without a destination in shared memory.
+__device__ inline void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)),
+               "r"(bytes)
+               : "memory");
+}
+
 __device__ inline void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -248,6 +256,16 @@ __device__ inline void st_async_v4(uint32_t caddr, uint32_t a, uint32_t b, uint3
   asm volatile(
       "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1,%2,%3,%4}, [%5];" ::"r"(caddr),
       "r"(a), "r"(b), "r"(c), "r"(d), "r"(cbar)
+      : "memory");
+}
+// Bulk copy (by the async copy engine) of `bytes` from this CTA's shared
+// memory to another CTA's; both addresses 16-byte aligned, `bytes` a multiple
+// of 16.  Completes `bytes` of transaction count on the mbarrier `cbar` of
+// the destination CTA (dst and cbar from mapa).
+__device__ inline void bulk_copy_to_peer(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t cbar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "r"(src), "r"(bytes), "r"(cbar)
       : "memory");
 }
 // Arrive on a barrier given by its shared::cluster address (from mapa).
