@@ -60,6 +60,7 @@ constexpr uint32_t kTmO = 0, kTmS = 256, kTmQ = 384;
 constexpr int kThreads = 512;
 constexpr float kRescaleLog2 = 8.f;  // lazy rescale threshold: P stays <= 2^8
 constexpr int kPrefetchPages = 6;    // L2 prefetch distance of the producer, in pages
+constexpr int kPageRing = 8;         // page ids read ahead by the prefetcher (> kPrefetchPages)
 
 enum {
   B_FULL = 0,
@@ -163,6 +164,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   __shared__ long long sh_P, sh_s0;
   __shared__ int sh_b0;
   __shared__ uint16_t mx_swap[2][2][128];  // row maxima between the two softmax warpgroups
+  __shared__ int page_ring[kPageRing];     // producer-private
 
   const uint32_t rank = cluster_rank(), peer = rank ^ 1u;
   const int w = blockIdx.x >> 1;
@@ -245,12 +247,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // L2 prefetch runs kPrefetchPages pages ahead of the TMA ring, so the
       // ring's loads hit L2; rank 0 fetches the whole latent page, rank 1
       // the rope page.
+      // The prefetcher also keeps the page ids it reads in a small ring, so
+      // the ring's loads need no global read of their own.
       bool pf_have = pf.next(a, pu);
       int pj = pf_have ? pu.pb : 0;
+      uint32_t pf_count = 0;
       auto prefetch_next = [&]() {
         if (!pf_have) return;
-        const int page = a.page_table[(size_t)pu.b * a.maxp + pj];
-        if (page >= 0 && page < a.num_pages) {
+        int page = a.page_table[(size_t)pu.b * a.maxp + pj];
+        if (page < 0 || page >= a.num_pages) page = -1;
+        page_ring[pf_count++ % kPageRing] = page;
+        if (page >= 0) {
           if (rank == 0)
             prefetch_l2(static_cast<const uint8_t*>(a.ckv) + (size_t)page * kPage * kLatent * 2,
                         kPage * kLatent * 2);
@@ -272,8 +279,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          int page = a.page_table[(size_t)u.b * a.maxp + j];
-          if (page < 0 || page >= a.num_pages) page = 0;  // masked by the softmax warps
+          int page = page_ring[g % kPageRing];
+          if (page < 0) page = 0;  // a bad page id: masked by the softmax warps
           const uint32_t st = base + s * kStageBytes;
           mbar_expect_tx(bar(B_FULL + s), tx);
 #pragma unroll
@@ -525,10 +532,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     while (ok && have) {
       const int np = u.pe - u.pb;
       float m = -INFINITY, l = 0.f;
+      const int32_t* ptab = a.page_table + (size_t)u.b * a.maxp;
+      int page_nx = ptab[u.pb];
       for (int i = 0; i < np; ++i) {
         const uint32_t gi = g + i, sb = gi & 1, s = gi % kStages;
         const int jp = u.pb + i;
-        const int page = a.page_table[(size_t)u.b * a.maxp + jp];
+        // page ids are read one page ahead: a global load's latency stays off
+        // the softmax's critical path
+        const int page = page_nx;
+        if (i + 1 < np) page_nx = ptab[jp + 1];
         const bool page_ok = page >= 0 && page < a.num_pages;
         const int valid = page_ok ? min(kPage, u.n - jp * kPage) : 0;
         if (!page_ok && h == 0 && j == 0 && rank == 0) set_error(a.err, MLA_ERR_PAGE_OOB);
