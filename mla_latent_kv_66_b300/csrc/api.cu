@@ -152,8 +152,7 @@ mla_status mla_decode(const mla_params* p, const void* q_lat, const void* q_pe,
   a.maxp = p->max_pages_per_seq;
   a.num_pages = p->num_pages;
   a.scale_log2 = p->softmax_scale * kLog2e;
-  return cuda_status(fp8 ? launch_decode_simt(a, (cudaStream_t)stream)
-                         : launch_decode_tc(a, (cudaStream_t)stream));
+  return cuda_status(launch_decode_tc(a, (cudaStream_t)stream));
 }
 
 mla_status mla_split_kv_combine(const mla_params* p, const void* workspace, size_t ws_bytes,

@@ -1,0 +1,93 @@
+// Split-KV combine: merge the partial results of sequences whose cache pages
+// were divided between several decode workers.
+//
+// Method (flash-decoding style log-sum-exp merge of attention over disjoint
+// token ranges; the page "DeepSeek-Coder-V2 的 MLA ... 512维潜空间" motivates
+// splitting with its 128K contexts): for the partials s of one (sequence,
+// head), o = sum_s exp(lse_s - L) O_s with L = log sum_s exp(lse_s), each O_s
+// normalised over its own range.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace mla {
+namespace {
+
+// One CTA per (sequence, head) of a split sequence; thread t owns latent
+// columns [4t, 4t+4).  The partials of the sequence are the records of the
+// workers whose page ranges it overlaps, in page order.  Their slots and
+// weights are worked out once per CTA (128 at a time) into shared memory.
+__global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ part_o,
+                                                      const float* __restrict__ part_lse,
+                                                      const int* __restrict__ seq_start,
+                                                      __nv_bfloat16* __restrict__ o_lat,
+                                                      float* __restrict__ lse_out, int B, int H, int G) {
+  __shared__ int s_slot[128];
+  __shared__ float s_val[128];
+  __shared__ float s_red[4];
+  const int b = blockIdx.x, h = blockIdx.y, t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const long long P = seq_start[B];
+  const long long sb = seq_start[b], se = seq_start[b + 1];
+  if (se <= sb) return;
+  const int wf = worker_of(sb, G, P), wl = worker_of(se - 1, G, P);
+  if (wf == wl) return;  // finished by the decode kernel
+  const int n = wl - wf + 1;
+  // slot of partial i, or -1 for an empty worker range (no partial written)
+  auto slot_of = [&](int i) {
+    const int w = wf + i;
+    const long long lo = range_lo(w, G, P), hi = range_lo(w + 1, G, P);
+    return lo == hi ? -1 : (sb <= lo ? w : G + w);
+  };
+  // pass 1: the largest partial log-sum-exp
+  float mx = -INFINITY;
+  for (int i = t; i < n; i += 128) {
+    const int sl = slot_of(i);
+    if (sl >= 0) mx = fmaxf(mx, part_lse[(size_t)sl * H + h]);
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if (lane == 0) s_red[warp] = mx;
+  __syncthreads();
+  mx = fmaxf(fmaxf(s_red[0], s_red[1]), fmaxf(s_red[2], s_red[3]));
+  // pass 2: weighted sum, 128 partials at a time
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float sum = 0.f;
+  for (int c0 = 0; c0 < n; c0 += 128) {
+    const int m = min(128, n - c0);
+    __syncthreads();  // the previous chunk's entries are no longer read
+    if (t < m) {
+      const int sl = slot_of(c0 + t);
+      const float l = sl >= 0 ? part_lse[(size_t)sl * H + h] : -INFINITY;
+      s_slot[t] = sl;
+      s_val[t] = l == -INFINITY ? 0.f : __expf(l - mx);
+    }
+    __syncthreads();
+#pragma unroll 4
+    for (int i = 0; i < m; ++i) {
+      const int sl = s_slot[i];
+      if (sl < 0) continue;
+      const float wt = s_val[i];
+      sum += wt;
+      const float4 v = reinterpret_cast<const float4*>(part_o + ((size_t)sl * H + h) * kLatent)[t];
+      acc.x = fmaf(wt, v.x, acc.x);
+      acc.y = fmaf(wt, v.y, acc.y);
+      acc.z = fmaf(wt, v.z, acc.z);
+      acc.w = fmaf(wt, v.w, acc.w);
+    }
+  }
+  const float inv = sum > 0.f ? 1.f / sum : 0.f;
+  __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(o_lat + ((size_t)b * H + h) * kLatent + 4 * t);
+  dst[0] = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+  dst[1] = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+  if (t == 0 && lse_out) lse_out[(size_t)b * H + h] = mx + logf(sum);
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const float* part_o, const float* part_lse, const int* seq_start,
+                           __nv_bfloat16* o_lat, float* lse, int B, int H, int G, cudaStream_t stream) {
+  dim3 grid(B, H);
+  combine_kernel<<<grid, 128, 0, stream>>>(part_o, part_lse, seq_start, o_lat, lse, B, H, G);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

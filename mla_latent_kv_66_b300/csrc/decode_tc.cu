@@ -47,15 +47,28 @@ namespace {
 
 using namespace tc;
 
-constexpr int kStages = 3;
-constexpr uint32_t kBox = 8192;             // [64 rows x 64 bf16], 128-byte swizzle
-constexpr uint32_t kStageBytes = 5 * kBox;  // 4 latent boxes + k_pe box (rank 1)
-constexpr uint32_t kOffQpe = kStages * kStageBytes;  // [128 x 64] bf16 (rank 1)
-constexpr uint32_t kOffP = kOffQpe + 16384;          // [128 x 64] bf16 probabilities
-constexpr uint32_t kOffX = kOffP + 16384;            // 2 x [128 x 64] fp16 peer partial scores
-constexpr uint32_t kXBytes = 16384;
-constexpr uint32_t kOffXs = kOffX + 2 * kXBytes;     // 2 x [128 x 64] fp16 own partial, outgoing
-constexpr uint32_t kSmemBytes = kOffXs + 2 * kXBytes + 1024;
+constexpr uint32_t kBox = 8192;            // [64 rows x 64 bf16], 128-byte swizzle
+constexpr uint32_t kStageBf = 5 * kBox;    // bf16 stage: 4 latent boxes + k_pe box (rank 1)
+constexpr uint32_t kXBytes = 16384;        // [128 x 64] fp16 partial-score tile
+// E4M3 cache: a raw page holds this CTA's 256 latent codes of 64 tokens as two
+// [64 x 128 B] boxes, the 64 rope codes (rank 1, [64 x 64 B]) and the page's
+// 64 fp32 scales; after expansion the bf16 stage also carries the scales.
+constexpr uint32_t kRawKpe = 2 * 8192, kRawScale = kRawKpe + 4096, kRawBytes = 21504;
+constexpr uint32_t kStageScale = kStageBf;
+constexpr int kMaxStages = 3;
+
+template <bool kFp8>
+struct Layout {
+  static constexpr int kStages = kFp8 ? 2 : 3;   // bf16 stages the MMAs read
+  static constexpr int kRaw = kFp8 ? 2 : 0;      // raw E4M3 pages
+  static constexpr uint32_t kStageBytes = kFp8 ? kStageBf + 1024 : kStageBf;
+  static constexpr uint32_t kOffRaw = kStages * kStageBytes;
+  static constexpr uint32_t kOffQpe = kOffRaw + kRaw * kRawBytes;  // [128 x 64] bf16 (rank 1)
+  static constexpr uint32_t kOffP = kOffQpe + 16384;               // [128 x 64] bf16 probabilities
+  static constexpr uint32_t kOffX = kOffP + 16384;                 // 2 x peer partial scores
+  static constexpr uint32_t kOffXs = kOffX + 2 * kXBytes;          // 2 x own partial, outgoing
+  static constexpr uint32_t kSmemBytes = kOffXs + 2 * kXBytes + 1024;
+};
 constexpr uint32_t kTmO = 0, kTmS = 256, kTmQ = 384;
 constexpr int kThreads = 512;
 constexpr float kRescaleLog2 = 8.f;  // lazy rescale threshold: P stays <= 2^8
@@ -63,9 +76,11 @@ constexpr int kPrefetchPages = 6;    // L2 prefetch distance of the producer, in
 constexpr int kPageRing = 8;         // page ids read ahead by the prefetcher (> kPrefetchPages)
 
 enum {
-  B_FULL = 0,
-  B_EMPTY = B_FULL + kStages,
-  B_SFULL = B_EMPTY + kStages,
+  B_FULL = 0,                       // bf16 stage ready (TMA landed, or E4M3 expanded)
+  B_EMPTY = B_FULL + kMaxStages,    // bf16 stage consumed by P . V
+  B_RFULL = B_EMPTY + kMaxStages,   // raw E4M3 page landed
+  B_RFREE = B_RFULL + 2,            // raw E4M3 page expanded
+  B_SFULL = B_RFREE + 2,
   B_SFREE = B_SFULL + 2,
   B_XFULL = B_SFREE + 2,
   B_XFREE = B_XFULL + 2,
@@ -134,6 +149,28 @@ __device__ inline uint4 ld_shared_v4u(uint32_t addr) {
                : "memory");
   return v;
 }
+// Two E4M3 codes (low 16 bits of v) as a bf16 pair, exactly: E4M3 -> f16
+// (hardware conversion) -> f32 -> bf16 loses nothing, every E4M3 value
+// having at most 4 significant bits and an exponent inside both ranges.
+__device__ inline uint32_t e4m3x2_to_bf16x2(uint32_t v) {
+  uint32_t h2;
+  asm("{\n .reg .b16 t;\n cvt.u16.u32 t, %1;\n cvt.rn.f16x2.e4m3x2 %0, t;\n}\n" : "=r"(h2) : "r"(v));
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+  return pack_bf16(f.x, f.y);
+}
+__device__ inline float4 ld_shared_v4f(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+__device__ inline float ld_shared_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
 __device__ inline float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -154,9 +191,14 @@ __device__ inline float2 unpack_h2(uint32_t u) {
   return __half22float2(*reinterpret_cast<const __half2*>(&u));
 }
 
+template <bool kFp8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_ckv,
                      const __grid_constant__ CUtensorMap tm_kpe, DecodeArgs a) {
+  using L = Layout<kFp8>;
+  constexpr int kStages = L::kStages;
+  constexpr uint32_t kStageBytes = L::kStageBytes;
+  constexpr uint32_t kOffQpe = L::kOffQpe, kOffP = L::kOffP, kOffX = L::kOffX, kOffXs = L::kOffXs;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bars[B_COUNT];
   __shared__ uint32_t tmem_slot;
@@ -175,8 +217,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(bar(B_FULL + i), 1);
+      mbar_init(bar(B_FULL + i), kFp8 ? 128 : 1);  // E4M3: the 128 expanding threads
       mbar_init(bar(B_EMPTY + i), 1);
+    }
+    for (int i = 0; i < L::kRaw; ++i) {
+      mbar_init(bar(B_RFULL + i), 1);
+      mbar_init(bar(B_RFREE + i), 128);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(B_SFULL + i), 1);
@@ -258,12 +304,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (page < 0 || page >= a.num_pages) page = -1;
         page_ring[pf_count++ % kPageRing] = page;
         if (page >= 0) {
+          constexpr uint32_t es = kFp8 ? 1 : 2;  // bytes per cached value
           if (rank == 0)
-            prefetch_l2(static_cast<const uint8_t*>(a.ckv) + (size_t)page * kPage * kLatent * 2,
-                        kPage * kLatent * 2);
+            prefetch_l2(static_cast<const uint8_t*>(a.ckv) + (size_t)page * kPage * kLatent * es,
+                        kPage * kLatent * es);
           else
-            prefetch_l2(static_cast<const uint8_t*>(a.kpe) + (size_t)page * kPage * kRope * 2,
-                        kPage * kRope * 2);
+            prefetch_l2(static_cast<const uint8_t*>(a.kpe) + (size_t)page * kPage * kRope * es,
+                        kPage * kRope * es);
+          if (kFp8 && rank == 1) prefetch_l2(a.kv_scale + (size_t)page * kPage, kPage * 4);
         }
         if (++pj >= pu.pe) {
           pf_have = pf.next(a, pu);
@@ -271,29 +319,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       };
       for (int i = 0; i < kPrefetchPages; ++i) prefetch_next();
+      // bf16: pages go straight into the stage ring.  E4M3: pages go into the
+      // raw ring (codes and scales) and the exchange warps expand them.
+      constexpr int kRing = kFp8 ? L::kRaw : kStages;
       while (ok && wk.next(a, u)) {
         for (int j = u.pb; j < u.pe; ++j, ++g) {
-          const uint32_t s = g % kStages;
-          if (g >= kStages &&
-              !mbar_wait(bar(B_EMPTY + s), ((g / kStages) - 1) & 1, &abort_flag, a.err)) {
+          const uint32_t s = g % kRing;
+          const int free_bar = kFp8 ? B_RFREE : B_EMPTY, full_bar = kFp8 ? B_RFULL : B_FULL;
+          if (g >= (uint32_t)kRing &&
+              !mbar_wait(bar(free_bar + s), ((g / kRing) - 1) & 1, &abort_flag, a.err)) {
             ok = false;
             break;
           }
           int page = page_ring[g % kPageRing];
           if (page < 0) page = 0;  // a bad page id: masked by the softmax warps
-          const uint32_t st = base + s * kStageBytes;
-          mbar_expect_tx(bar(B_FULL + s), tx);
+          const uint32_t fb = bar(full_bar + s);
+          if (kFp8) {
+            const uint32_t raw = base + L::kOffRaw + s * kRawBytes;
+            mbar_expect_tx(fb, 2 * 8192 + (rank == 1 ? 4096 : 0) + kPage * 4);
+            tma_load_2d(raw, &tm_ckv, fb, (int)rank * 256, page * kPage);
+            tma_load_2d(raw + 8192, &tm_ckv, fb, (int)rank * 256 + 128, page * kPage);
+            if (rank == 1) tma_load_2d(raw + kRawKpe, &tm_kpe, fb, 0, page * kPage);
+            bulk_copy_g2s(raw + kRawScale, a.kv_scale + (size_t)page * kPage, kPage * 4, fb);
+          } else {
+            const uint32_t st = base + s * kStageBytes;
+            mbar_expect_tx(fb, tx);
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            tma_load_2d(st + i * kBox, &tm_ckv, bar(B_FULL + s), (int)rank * 256 + i * 64, page * kPage);
-          if (rank == 1) tma_load_2d(st + 4 * kBox, &tm_kpe, bar(B_FULL + s), 0, page * kPage);
+            for (int i = 0; i < 4; ++i)
+              tma_load_2d(st + i * kBox, &tm_ckv, fb, (int)rank * 256 + i * 64, page * kPage);
+            if (rank == 1) tma_load_2d(st + 4 * kBox, &tm_kpe, fb, 0, page * kPage);
+          }
           prefetch_next();
         }
       }
       // copies still in flight must land before the CTA can exit
-      for (uint32_t k = g > (uint32_t)kStages ? g - kStages : 0; k < g; ++k) {
+      for (uint32_t k = g > (uint32_t)kRing ? g - kRing : 0; k < g; ++k) {
         volatile int no_abort = 0;
-        mbar_wait(bar(B_FULL + k % kStages), (k / kStages) & 1, &no_abort, nullptr);
+        mbar_wait(bar((kFp8 ? B_RFULL : B_FULL) + k % kRing), (k / kRing) & 1, &no_abort, nullptr);
       }
     }
   } else if (warp == 1) {
@@ -416,10 +478,56 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t x_peer = mapa(base + kOffX, peer);
     const uint32_t xfull_peer0 = mapa(bar(B_XFULL), peer);
     const float c = a.scale_log2;
+    const long long lo = range_lo(w, a.G, P), hi = range_lo(w + 1, a.G, P);
+    const uint32_t npages = hi > lo ? (uint32_t)(hi - lo) : 0u;
+
+    // E4M3 only: expand raw page gc into bf16 stage gc % kStages (exact
+    // conversion, same 128-byte-swizzled layout TMA gives the bf16 cache) and
+    // copy its scales.  Thread h converts 16 codes per step.
+    constexpr uint32_t kRawN = L::kRaw > 0 ? L::kRaw : 1;
+    auto expand = [&](uint32_t gc) -> bool {
+      const uint32_t r = gc % kRawN, s = gc % kStages;
+      if (!wwait(B_RFULL + r, (gc / kRawN) & 1)) return false;
+      if (gc >= (uint32_t)kStages && !wwait(B_EMPTY + s, ((gc / kStages) - 1) & 1)) return false;
+      const uint32_t raw = base + L::kOffRaw + r * kRawBytes, st = base + s * kStageBytes;
+#pragma unroll 2
+      for (int i = 0; i < 8; ++i) {  // latent: 2 boxes x 64 rows x 8 chunks of 16 codes
+        const int q = h + 128 * i, box = q >> 9, row = (q >> 3) & 63, cc = q & 7;
+        const uint4 v = ld_shared_v4u(raw + box * 8192 + row * 128 + cc * 16);
+        const int col = box * 128 + cc * 16, kb = col >> 6, cb = (col & 63) >> 3;
+        const uint32_t rowa = st + kb * kBox + row * 128;
+        st_shared_v4(rowa + ((cb ^ (row & 7)) << 4), e4m3x2_to_bf16x2(v.x), e4m3x2_to_bf16x2(v.x >> 16),
+                     e4m3x2_to_bf16x2(v.y), e4m3x2_to_bf16x2(v.y >> 16));
+        st_shared_v4(rowa + (((cb + 1) ^ (row & 7)) << 4), e4m3x2_to_bf16x2(v.z), e4m3x2_to_bf16x2(v.z >> 16),
+                     e4m3x2_to_bf16x2(v.w), e4m3x2_to_bf16x2(v.w >> 16));
+      }
+      if (rank == 1) {  // rope codes: 64 rows x 4 chunks
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int q = h + 128 * i, row = q >> 2, cc = q & 3;
+          const uint4 v = ld_shared_v4u(raw + kRawKpe + row * 64 + cc * 16);
+          const uint32_t rowa = st + 4 * kBox + row * 128;
+          st_shared_v4(rowa + (((2 * cc) ^ (row & 7)) << 4), e4m3x2_to_bf16x2(v.x),
+                       e4m3x2_to_bf16x2(v.x >> 16), e4m3x2_to_bf16x2(v.y), e4m3x2_to_bf16x2(v.y >> 16));
+          st_shared_v4(rowa + (((2 * cc + 1) ^ (row & 7)) << 4), e4m3x2_to_bf16x2(v.z),
+                       e4m3x2_to_bf16x2(v.z >> 16), e4m3x2_to_bf16x2(v.w), e4m3x2_to_bf16x2(v.w >> 16));
+        }
+      }
+      if (h < kPage / 4) {
+        const uint4 v = ld_shared_v4u(raw + kRawScale + h * 16);
+        st_shared_v4(st + kStageScale + h * 16, v.x, v.y, v.z, v.w);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(bar(B_FULL + s));
+      mbar_arrive(bar(B_RFREE + r));
+      return true;
+    };
+
     Walker wk = walker0;
     Unit u;
     uint32_t g = 0;
     bool ok = true;
+    if (kFp8 && npages > 0) ok = expand(0);
     while (ok && wk.next(a, u)) {
       for (int jp = u.pb; jp < u.pe; ++jp, ++g) {
         const uint32_t sb = g & 1;
@@ -451,6 +559,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           else bulk_copy_to_peer(x_peer + sb * kXBytes, stg, kXBytes, xfull_peer0 + sb * 8);
         }
         if (!__all_sync(0xffffffffu, ok)) break;
+        // the next page's expansion waits for the P . V that frees its stage,
+        // so it comes after this page's exchange
+        if (kFp8 && g + 1 < npages && !expand(g + 1)) { ok = false; break; }
       }
     }
   } else {
@@ -569,6 +680,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
         mbar_arrive(bar(B_XREAD + sb));  // relayed to the peer by warp 2
+        // E4M3: the score of token t is scale_t times the score of its codes
+        const uint32_t sca = base + s * kStageBytes + kStageScale + j * 128;
+        if constexpr (kFp8) {
+          if (!wwait(B_FULL + s, (gi / kStages) & 1)) { ok = false; break; }  // scales visible
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float4 v = ld_shared_v4f(sca + q * 16);
+            x[4 * q] *= v.x;
+            x[4 * q + 1] *= v.y;
+            x[4 * q + 2] *= v.z;
+            x[4 * q + 3] *= v.w;
+          }
+        }
         if (valid < kPage) {  // tokens past the sequence end (or a bad page)
 #pragma unroll
           for (int k = 0; k < 32; ++k) x[k] = 32 * j + k < valid ? x[k] : -INFINITY;
@@ -602,7 +726,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int k = 0; k < 16; ++k) {
           const float p0 = ex2(x[2 * k] - mm), p1 = ex2(x[2 * k + 1] - mm);
           ps[k & 3] += p0 + p1;
-          pk[k] = pack_bf16(p0, p1);
+          if constexpr (kFp8) {
+            // P . V multiplies codes: fold each token's scale into its
+            // probability (0 past the end, where the scale may be garbage)
+            float s0 = 0.f, s1 = 0.f;
+            if (32 * j + 2 * k < valid) s0 = ld_shared_f32(sca + 8 * k);
+            if (32 * j + 2 * k + 1 < valid) s1 = ld_shared_f32(sca + 8 * k + 4);
+            pk[k] = pack_bf16(p0 * s0, p1 * s1);
+          } else {
+            pk[k] = pack_bf16(p0, p1);
+          }
         }
         l = l * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
 
@@ -715,33 +848,48 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 // Clusters of the decode kernel that fit on the device at once (0 on error).
 int decode_tc_max_clusters() {
-  if (cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)kSmemBytes) != cudaSuccess)
+  constexpr uint32_t smem = Layout<false>::kSmemBytes;
+  if (cudaFuncSetAttribute(decode_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem) != cudaSuccess)
     return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = smem;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, decode_tc_kernel, &cfg) != cudaSuccess) return 0;
+  if (cudaOccupancyMaxActiveClusters(&n, decode_tc_kernel<false>, &cfg) != cudaSuccess) return 0;
   return n;
 }
 
+// bf16 cache: tiles TMA-loaded straight into the 128-byte-swizzled stages.
+// E4M3 cache (kv_scale != null): raw tiles without swizzle, expanded in the
+// kernel.
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t stream) {
-  if ((reinterpret_cast<uintptr_t>(a.ckv) & 15) || (reinterpret_cast<uintptr_t>(a.kpe) & 15))
+  const bool fp8 = a.kv_scale != nullptr;
+  if ((reinterpret_cast<uintptr_t>(a.ckv) & 15) || (reinterpret_cast<uintptr_t>(a.kpe) & 15) ||
+      (reinterpret_cast<uintptr_t>(a.kv_scale) & 15))
     return cudaErrorInvalidValue;
   CUtensorMap tc_map, tk_map;
   const cuuint64_t rows = (cuuint64_t)a.num_pages * kPage;
-  const cuuint64_t cd[2] = {kLatent, rows}, cs[1] = {kLatent * 2};
-  const cuuint64_t kd[2] = {kRope, rows}, ks[1] = {kRope * 2};
-  const cuuint32_t box[2] = {64, 64};
-  if (!make_tmap(&tc_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.ckv, cd, cs, box) ||
-      !make_tmap(&tk_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.kpe, kd, ks, box))
-    return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)kSmemBytes);
+  const cuuint64_t es = fp8 ? 1 : 2;
+  const cuuint64_t cd[2] = {kLatent, rows}, cs[1] = {kLatent * es};
+  const cuuint64_t kd[2] = {kRope, rows}, ks[1] = {kRope * es};
+  if (fp8) {
+    const cuuint32_t cbox[2] = {128, 64}, kbox[2] = {64, 64};
+    if (!make_tmap(&tc_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.ckv, cd, cs, cbox, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_tmap(&tk_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.kpe, kd, ks, kbox, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return cudaErrorInvalidValue;
+  } else {
+    const cuuint32_t box[2] = {64, 64};
+    if (!make_tmap(&tc_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.ckv, cd, cs, box) ||
+        !make_tmap(&tk_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.kpe, kd, ks, box))
+      return cudaErrorInvalidValue;
+  }
+  auto kernel = fp8 ? decode_tc_kernel<true> : decode_tc_kernel<false>;
+  const uint32_t smem = fp8 ? Layout<true>::kSmemBytes : Layout<false>::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  decode_tc_kernel<<<2 * a.G, kThreads, kSmemBytes, stream>>>(tc_map, tk_map, a);
+  kernel<<<2 * a.G, kThreads, smem, stream>>>(tc_map, tk_map, a);
   return cudaGetLastError();
 }
 

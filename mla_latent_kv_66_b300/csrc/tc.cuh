@@ -268,6 +268,14 @@ __device__ inline void bulk_copy_to_peer(uint32_t dst, uint32_t src, uint32_t by
       "r"(src), "r"(bytes), "r"(cbar)
       : "memory");
 }
+// Bulk copy (async copy engine) of `bytes` from global memory into this
+// CTA's shared memory, completing `bytes` of transaction count on `bar`;
+// both addresses 16-byte aligned, `bytes` a multiple of 16.
+__device__ inline void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
 // Arrive on a barrier given by its shared::cluster address (from mapa).
 __device__ inline void mbar_arrive_remote(uint32_t caddr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr)

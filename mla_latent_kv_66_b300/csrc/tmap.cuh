@@ -23,15 +23,16 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
   return fn;
 }
 
-// Tiled map with 128-byte swizzle.  dims/box are innermost first; strides are
+// Tiled map, 128-byte swizzle unless asked otherwise.  dims/box are innermost first; strides are
 // the byte strides of dims 1..rank-1.  Out-of-bounds boxes read zeros.
 inline bool make_tmap(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base,
-                      const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box) {
+                      const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
+                      CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto enc = tmap_encoder();
   if (!enc) return false;
   cuuint32_t es[5] = {1, 1, 1, 1, 1};
   CUresult r = enc(m, dt, (cuuint32_t)rank, const_cast<void*>(base), dims, strides, box, es,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
