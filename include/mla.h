@@ -119,7 +119,7 @@ int mla_decode_num_splits(const mla_params* p, int num_splits);
  *        unit holding its last page when that is another unit (else seq=-1)
  *   [2]  int32 page offset of each sequence, B+1 entries
  *   [3]  partial LSE, fp32 [2*G, H]
- *   [4]  partial O, fp32 [2*G, H, 512], normalised
+ *   [4]  partial O, bf16 [2*G, H, 512], normalised
  */
 size_t mla_decode_workspace_size(const mla_params* p, int num_splits);
 void mla_workspace_offsets(const mla_params* p, int num_splits, size_t offsets[5]);

@@ -145,7 +145,7 @@ mla_status mla_decode(const mla_params* p, const void* q_lat, const void* q_pe,
   a.rec = reinterpret_cast<int4*>(ws + l.rec);
   a.seq_start = reinterpret_cast<int*>(ws + l.seq_start);
   a.part_lse = reinterpret_cast<float*>(ws + l.part_lse);
-  a.part_o = reinterpret_cast<float*>(ws + l.part_o);
+  a.part_o = reinterpret_cast<__nv_bfloat16*>(ws + l.part_o);
   a.B = p->B;
   a.H = p->H;
   a.G = G;
@@ -165,7 +165,7 @@ mla_status mla_split_kv_combine(const mla_params* p, const void* workspace, size
   const WsLayout l = ws_layout(p->B, p->H, G);
   if (!workspace || ws_bytes < l.total) return MLA_ERR_WORKSPACE;
   const uint8_t* ws = static_cast<const uint8_t*>(workspace);
-  return cuda_status(launch_combine(reinterpret_cast<const float*>(ws + l.part_o),
+  return cuda_status(launch_combine(reinterpret_cast<const __nv_bfloat16*>(ws + l.part_o),
                                     reinterpret_cast<const float*>(ws + l.part_lse),
                                     reinterpret_cast<const int*>(ws + l.seq_start),
                                     static_cast<__nv_bfloat16*>(o_lat), lse, p->B, p->H, G,

@@ -16,7 +16,7 @@ namespace {
 // columns [4t, 4t+4).  The partials of the sequence are the records of the
 // workers whose page ranges it overlaps, in page order.  Their slots and
 // weights are worked out once per CTA (128 at a time) into shared memory.
-__global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ part_o,
+__global__ void __launch_bounds__(128) combine_kernel(const __nv_bfloat16* __restrict__ part_o,
                                                       const float* __restrict__ part_lse,
                                                       const int* __restrict__ seq_start,
                                                       __nv_bfloat16* __restrict__ o_lat,
@@ -67,11 +67,11 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
       if (sl < 0) continue;
       const float wt = s_val[i];
       sum += wt;
-      const float4 v = reinterpret_cast<const float4*>(part_o + ((size_t)sl * H + h) * kLatent)[t];
-      acc.x = fmaf(wt, v.x, acc.x);
-      acc.y = fmaf(wt, v.y, acc.y);
-      acc.z = fmaf(wt, v.z, acc.z);
-      acc.w = fmaf(wt, v.w, acc.w);
+      const uint2 v = reinterpret_cast<const uint2*>(part_o + ((size_t)sl * H + h) * kLatent)[t];
+      acc.x = fmaf(wt, bf16lo(v.x), acc.x);
+      acc.y = fmaf(wt, bf16hi(v.x), acc.y);
+      acc.z = fmaf(wt, bf16lo(v.y), acc.z);
+      acc.w = fmaf(wt, bf16hi(v.y), acc.w);
     }
   }
   const float inv = sum > 0.f ? 1.f / sum : 0.f;
@@ -83,7 +83,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
 
 }  // namespace
 
-cudaError_t launch_combine(const float* part_o, const float* part_lse, const int* seq_start,
+cudaError_t launch_combine(const __nv_bfloat16* part_o, const float* part_lse, const int* seq_start,
                            __nv_bfloat16* o_lat, float* lse, int B, int H, int G, cudaStream_t stream) {
   dim3 grid(B, H);
   combine_kernel<<<grid, 128, 0, stream>>>(part_o, part_lse, seq_start, o_lat, lse, B, H, G);

@@ -36,7 +36,7 @@ __host__ __device__ inline WsLayout ws_layout(int B, int H, int G) {
   l.seq_start = align_up(l.rec + (size_t)2 * G * 16, 256);
   l.part_lse = align_up(l.seq_start + (size_t)(B + 1) * 4, 256);
   l.part_o = align_up(l.part_lse + (size_t)2 * G * H * 4, 256);
-  l.total = align_up(l.part_o + (size_t)2 * G * H * kLatent * 4, 256);
+  l.total = align_up(l.part_o + (size_t)2 * G * H * kLatent * 2, 256);
   return l;
 }
 
@@ -54,7 +54,7 @@ struct DecodeArgs {
   int4* rec;                   // [2G]
   int* seq_start;              // [B+1]
   float* part_lse;             // [2G,H]
-  float* part_o;               // [2G,H,512]
+  __nv_bfloat16* part_o;       // [2G,H,512], normalised
   int B, H, G, maxp, num_pages;
   float scale_log2;            // softmax_scale * log2(e)
 };

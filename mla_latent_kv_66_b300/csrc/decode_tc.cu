@@ -73,7 +73,7 @@ constexpr uint32_t kTmO = 0, kTmS = 256, kTmQ = 384;
 constexpr int kThreads = 512;
 constexpr float kRescaleLog2 = 8.f;  // lazy rescale threshold: P stays <= 2^8
 constexpr int kPrefetchPages = 6;    // L2 prefetch distance of the producer, in pages
-constexpr int kPageRing = 8;         // page ids read ahead by the prefetcher (> kPrefetchPages)
+constexpr int kIdRing = 16;          // page ids copied ahead by the producer (> kPrefetchPages)
 
 enum {
   B_FULL = 0,                       // bf16 stage ready (TMA landed, or E4M3 expanded)
@@ -206,7 +206,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   __shared__ long long sh_P, sh_s0;
   __shared__ int sh_b0;
   __shared__ uint16_t mx_swap[2][2][128];  // row maxima between the two softmax warpgroups
-  __shared__ int page_ring[kPageRing];     // producer-private
+  __shared__ int page_ids[kIdRing];        // producer-private
 
   const uint32_t rank = cluster_rank(), peer = rank ^ 1u;
   const int w = blockIdx.x >> 1;
@@ -285,40 +285,53 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      Walker wk = walker0, pf = walker0;
-      Unit u, pu;
+      Walker wk = walker0;
+      Unit u;
       uint32_t g = 0;
       bool ok = true;
       const uint32_t tx = rank == 0 ? 4 * kBox : 5 * kBox;
+      const long long lo = range_lo(w, a.G, P), hi = range_lo(w + 1, a.G, P);
+      const uint32_t npages = hi > lo ? (uint32_t)(hi - lo) : 0u;
+      // Page ids travel global -> shared by asynchronous 4-byte copies kIdRing
+      // positions ahead, so no load latency sits in this loop: the id of the
+      // worker's k-th page lands in page_ids[k % kIdRing] with copy group k.
+      Walker idw = walker0;
+      Unit iu;
+      bool id_have = idw.next(a, iu);
+      int ij = id_have ? iu.pb : 0;
+      uint32_t id_count = 0;
+      auto id_fetch = [&]() {
+        if (id_have) {
+          cp_async_4(smem_u32(&page_ids[id_count % kIdRing]), a.page_table + (size_t)iu.b * a.maxp + ij);
+          if (++ij >= iu.pe) {
+            id_have = idw.next(a, iu);
+            ij = id_have ? iu.pb : 0;
+          }
+        }
+        cp_async_commit();
+        ++id_count;
+      };
+      auto page_at = [&](uint32_t k) {
+        const int pg = page_ids[k % kIdRing];
+        return pg >= 0 && pg < a.num_pages ? pg : -1;
+      };
       // L2 prefetch runs kPrefetchPages pages ahead of the TMA ring, so the
       // ring's loads hit L2; rank 0 fetches the whole latent page, rank 1
-      // the rope page.
-      // The prefetcher also keeps the page ids it reads in a small ring, so
-      // the ring's loads need no global read of their own.
-      bool pf_have = pf.next(a, pu);
-      int pj = pf_have ? pu.pb : 0;
-      uint32_t pf_count = 0;
-      auto prefetch_next = [&]() {
-        if (!pf_have) return;
-        int page = a.page_table[(size_t)pu.b * a.maxp + pj];
-        if (page < 0 || page >= a.num_pages) page = -1;
-        page_ring[pf_count++ % kPageRing] = page;
-        if (page >= 0) {
-          constexpr uint32_t es = kFp8 ? 1 : 2;  // bytes per cached value
-          if (rank == 0)
-            prefetch_l2(static_cast<const uint8_t*>(a.ckv) + (size_t)page * kPage * kLatent * es,
-                        kPage * kLatent * es);
-          else
-            prefetch_l2(static_cast<const uint8_t*>(a.kpe) + (size_t)page * kPage * kRope * es,
-                        kPage * kRope * es);
-          if (kFp8 && rank == 1) prefetch_l2(a.kv_scale + (size_t)page * kPage, kPage * 4);
-        }
-        if (++pj >= pu.pe) {
-          pf_have = pf.next(a, pu);
-          pj = pf_have ? pu.pb : 0;
-        }
+      // the rope page (and, for E4M3, the scales).
+      auto prefetch_page = [&](int page) {
+        if (page < 0) return;
+        constexpr uint32_t es = kFp8 ? 1 : 2;  // bytes per cached value
+        if (rank == 0)
+          prefetch_l2(static_cast<const uint8_t*>(a.ckv) + (size_t)page * kPage * kLatent * es,
+                      kPage * kLatent * es);
+        else
+          prefetch_l2(static_cast<const uint8_t*>(a.kpe) + (size_t)page * kPage * kRope * es,
+                      kPage * kRope * es);
+        if (kFp8 && rank == 1) prefetch_l2(a.kv_scale + (size_t)page * kPage, kPage * 4);
       };
-      for (int i = 0; i < kPrefetchPages; ++i) prefetch_next();
+      for (int i = 0; i < kIdRing; ++i) id_fetch();
+      cp_async_wait<0>();
+      for (uint32_t k = 0; k < (uint32_t)kPrefetchPages && k < npages; ++k) prefetch_page(page_at(k));
       // bf16: pages go straight into the stage ring.  E4M3: pages go into the
       // raw ring (codes and scales) and the exchange warps expand them.
       constexpr int kRing = kFp8 ? L::kRaw : kStages;
@@ -331,7 +344,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          int page = page_ring[g % kPageRing];
+          int page = page_at(g);
           if (page < 0) page = 0;  // a bad page id: masked by the softmax warps
           const uint32_t fb = bar(full_bar + s);
           if (kFp8) {
@@ -349,9 +362,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               tma_load_2d(st + i * kBox, &tm_ckv, fb, (int)rank * 256 + i * 64, page * kPage);
             if (rank == 1) tma_load_2d(st + 4 * kBox, &tm_kpe, fb, 0, page * kPage);
           }
-          prefetch_next();
+          // keep the L2 prefetch kPrefetchPages and the id copies kIdRing ahead
+          cp_async_wait<kIdRing - 1 - kPrefetchPages>();  // id of page g + kPrefetchPages landed
+          if (g + kPrefetchPages < npages) prefetch_page(page_at(g + kPrefetchPages));
+          id_fetch();  // page g + kIdRing, into the slot page g has left
         }
       }
+      cp_async_wait<0>();
       // copies still in flight must land before the CTA can exit
       for (uint32_t k = g > (uint32_t)kRing ? g - kRing : 0; k < g; ++k) {
         volatile int no_abort = 0;
@@ -802,21 +819,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tmem_ld32(tmem + lane_base + kTmO + j * 128 + cc * 32, r);
         tmem_wait_ld();
         if (h < H) {
-          if (!u.split) {
-            uint4* dst = reinterpret_cast<uint4*>(a.o_lat + row * kLatent + col0 + cc * 32);
+          // a whole sequence goes to o_lat, a split one to its partial slot
+          __nv_bfloat16* dst_row = u.split ? a.part_o + prow * kLatent : a.o_lat + row * kLatent;
+          uint4* dst = reinterpret_cast<uint4*>(dst_row + col0 + cc * 32);
 #pragma unroll
-            for (int v = 0; v < 4; ++v)
-              dst[v] = make_uint4(pack_bf16(__uint_as_float(r[8 * v]) * inv, __uint_as_float(r[8 * v + 1]) * inv),
-                                  pack_bf16(__uint_as_float(r[8 * v + 2]) * inv, __uint_as_float(r[8 * v + 3]) * inv),
-                                  pack_bf16(__uint_as_float(r[8 * v + 4]) * inv, __uint_as_float(r[8 * v + 5]) * inv),
-                                  pack_bf16(__uint_as_float(r[8 * v + 6]) * inv, __uint_as_float(r[8 * v + 7]) * inv));
-          } else {
-            float4* dst = reinterpret_cast<float4*>(a.part_o + prow * kLatent + col0 + cc * 32);
-#pragma unroll
-            for (int v = 0; v < 8; ++v)
-              dst[v] = make_float4(__uint_as_float(r[4 * v]) * inv, __uint_as_float(r[4 * v + 1]) * inv,
-                                   __uint_as_float(r[4 * v + 2]) * inv, __uint_as_float(r[4 * v + 3]) * inv);
-          }
+          for (int v = 0; v < 4; ++v)
+            dst[v] = make_uint4(pack_bf16(__uint_as_float(r[8 * v]) * inv, __uint_as_float(r[8 * v + 1]) * inv),
+                                pack_bf16(__uint_as_float(r[8 * v + 2]) * inv, __uint_as_float(r[8 * v + 3]) * inv),
+                                pack_bf16(__uint_as_float(r[8 * v + 4]) * inv, __uint_as_float(r[8 * v + 5]) * inv),
+                                pack_bf16(__uint_as_float(r[8 * v + 6]) * inv, __uint_as_float(r[8 * v + 7]) * inv));
         }
       }
       if (rank == 0 && j == 0 && h < H) {

@@ -6,7 +6,7 @@ namespace mla {
 
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t stream);
 int decode_tc_max_clusters();
-cudaError_t launch_combine(const float* part_o, const float* part_lse, const int* seq_start,
+cudaError_t launch_combine(const __nv_bfloat16* part_o, const float* part_lse, const int* seq_start,
                            __nv_bfloat16* o_lat, float* lse, int B, int H, int G, cudaStream_t stream);
 cudaError_t launch_absorb_tc(const __nv_bfloat16* q_nope, const __nv_bfloat16* w_uk,
                              __nv_bfloat16* q_lat, int B, int H, cudaStream_t stream);

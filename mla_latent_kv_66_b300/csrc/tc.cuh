@@ -126,6 +126,19 @@ __device__ inline void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// 4-byte asynchronous copy global -> shared (no register dependency), one
+// commit group per call of cp_async_commit; cp_async_wait<N> returns once at
+// most N of this thread's most recent groups are still in flight.
+__device__ inline void cp_async_4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src))
+               : "memory");
+}
+__device__ inline void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ inline void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // Make generic-proxy writes to shared memory visible to the async proxy
 // (tensor core operand reads).
 __device__ inline void fence_proxy_async_smem() {

@@ -46,7 +46,7 @@ def test_workspace_layout_matches_the_documented_formula():
     seq = up(rec + 2 * G * 16)
     lse = up(seq + (7 + 1) * 4)
     po = up(lse + 2 * G * 128 * 4)
-    total = up(po + 2 * G * 128 * 512 * 4)
+    total = up(po + 2 * G * 128 * 512 * 2)
     assert L.mla_workspace_offsets(p, G) == [0, rec, seq, lse, po]
     assert L.mla_decode_workspace_size(p, G) == total
 
