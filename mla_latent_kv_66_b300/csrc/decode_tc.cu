@@ -292,23 +292,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t tx = rank == 0 ? 4 * kBox : 5 * kBox;
       const long long lo = range_lo(w, a.G, P), hi = range_lo(w + 1, a.G, P);
       const uint32_t npages = hi > lo ? (uint32_t)(hi - lo) : 0u;
-      // Page ids travel global -> shared by asynchronous 4-byte copies kIdRing
-      // positions ahead, so no load latency sits in this loop: the id of the
-      // worker's k-th page lands in page_ids[k % kIdRing] with copy group k.
+      // Page ids are read kIdRing positions ahead of the ring: the id of the
+      // worker's k-th page is kept in page_ids[k % kIdRing].  The first
+      // kIdRing ids are loaded together; afterwards one load per page is
+      // issued and stored one page later, so no load latency sits in the loop.
       Walker idw = walker0;
       Unit iu;
       bool id_have = idw.next(a, iu);
       int ij = id_have ? iu.pb : 0;
-      uint32_t id_count = 0;
-      auto id_fetch = [&]() {
-        if (id_have) {
-          cp_async_4(smem_u32(&page_ids[id_count % kIdRing]), a.page_table + (size_t)iu.b * a.maxp + ij);
-          if (++ij >= iu.pe) {
-            id_have = idw.next(a, iu);
-            ij = id_have ? iu.pb : 0;
-          }
+      auto id_next = [&]() -> const int32_t* {  // address of the next id, null past the end
+        if (!id_have) return nullptr;
+        const int32_t* p = a.page_table + (size_t)iu.b * a.maxp + ij;
+        if (++ij >= iu.pe) {
+          id_have = idw.next(a, iu);
+          ij = id_have ? iu.pb : 0;
         }
-        cp_async_commit();
+        return p;
+      };
+      {
+        const int32_t* ptr[kIdRing];
+#pragma unroll
+        for (int i = 0; i < kIdRing; ++i) ptr[i] = id_next();
+        int v[kIdRing];
+#pragma unroll
+        for (int i = 0; i < kIdRing; ++i) v[i] = ptr[i] ? __ldg(ptr[i]) : -1;
+#pragma unroll
+        for (int i = 0; i < kIdRing; ++i) page_ids[i] = v[i];
+      }
+      uint32_t id_count = kIdRing;  // ids loaded so far (one more may be in flight)
+      int id_pend = -1;
+      bool id_pend_ok = false;
+      auto id_fetch = [&]() {
+        if (id_pend_ok) page_ids[(id_count - 1) % kIdRing] = id_pend;  // loaded one page ago
+        const int32_t* p = id_next();
+        id_pend_ok = true;
+        id_pend = p ? __ldg(p) : -1;
         ++id_count;
       };
       auto page_at = [&](uint32_t k) {
@@ -329,8 +347,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                       kPage * kRope * es);
         if (kFp8 && rank == 1) prefetch_l2(a.kv_scale + (size_t)page * kPage, kPage * 4);
       };
-      for (int i = 0; i < kIdRing; ++i) id_fetch();
-      cp_async_wait<0>();
       for (uint32_t k = 0; k < (uint32_t)kPrefetchPages && k < npages; ++k) prefetch_page(page_at(k));
       // bf16: pages go straight into the stage ring.  E4M3: pages go into the
       // raw ring (codes and scales) and the exchange warps expand them.
@@ -362,13 +378,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               tma_load_2d(st + i * kBox, &tm_ckv, fb, (int)rank * 256 + i * 64, page * kPage);
             if (rank == 1) tma_load_2d(st + 4 * kBox, &tm_kpe, fb, 0, page * kPage);
           }
-          // keep the L2 prefetch kPrefetchPages and the id copies kIdRing ahead
-          cp_async_wait<kIdRing - 1 - kPrefetchPages>();  // id of page g + kPrefetchPages landed
+          // keep the L2 prefetch kPrefetchPages and the page ids kIdRing ahead
           if (g + kPrefetchPages < npages) prefetch_page(page_at(g + kPrefetchPages));
-          id_fetch();  // page g + kIdRing, into the slot page g has left
+          id_fetch();  // stores the id of page g + kIdRing - 1, loads the next one
         }
       }
-      cp_async_wait<0>();
       // copies still in flight must land before the CTA can exit
       for (uint32_t k = g > (uint32_t)kRing ? g - kRing : 0; k < g; ++k) {
         volatile int no_abort = 0;
@@ -622,28 +636,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     auto load_q = [&](const Unit& q) {
       // this warpgroup's 128 latent values of the query half -> tensor memory
       // columns [64j, 64j+64) (two bf16 per column); q_pe -> shared memory
+      // every load is issued before the first store, so the two global
+      // round trips (latent and rope part) overlap
       const uint4* src = reinterpret_cast<const uint4*>(
           a.q_lat + ((size_t)q.b * H + h) * kLatent + rank * 256 + j * 128);
+      const uint4* sp = reinterpret_cast<const uint4*>(a.q_pe + ((size_t)q.b * H + h) * kRope);
+      const bool with_pe = rank == 1 && j == 0;
+      uint4 xq[16], xp[8];
+#pragma unroll
+      for (int v = 0; v < 16; ++v) xq[v] = h < H ? src[v] : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int v = 0; v < 8; ++v) xp[v] = with_pe && h < H ? sp[v] : make_uint4(0, 0, 0, 0);
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         uint32_t r[32];
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
-          uint4 x = h < H ? src[cc * 8 + v] : make_uint4(0, 0, 0, 0);
-          r[4 * v] = x.x;
-          r[4 * v + 1] = x.y;
-          r[4 * v + 2] = x.z;
-          r[4 * v + 3] = x.w;
+          r[4 * v] = xq[cc * 8 + v].x;
+          r[4 * v + 1] = xq[cc * 8 + v].y;
+          r[4 * v + 2] = xq[cc * 8 + v].z;
+          r[4 * v + 3] = xq[cc * 8 + v].w;
         }
         tmem_st32(tmem + lane_base + kTmQ + j * 64 + cc * 32, r);
       }
-      if (rank == 1 && j == 0) {
-        const uint4* sp = reinterpret_cast<const uint4*>(a.q_pe + ((size_t)q.b * H + h) * kRope);
+      if (with_pe) {
 #pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
-          uint4 x = h < H ? sp[cc] : make_uint4(0, 0, 0, 0);
-          st_shared_v4(base + kOffQpe + h * 128 + ((cc ^ (h & 7)) * 16), x.x, x.y, x.z, x.w);
-        }
+        for (int cc = 0; cc < 8; ++cc)
+          st_shared_v4(base + kOffQpe + h * 128 + ((cc ^ (h & 7)) * 16), xp[cc].x, xp[cc].y, xp[cc].z, xp[cc].w);
       }
       tmem_wait_st();
       fence_proxy_async_smem();
