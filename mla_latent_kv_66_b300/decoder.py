@@ -1,6 +1,8 @@
 """One MLA decode step over a resident paged latent cache, through the C ABI:
 absorb the query (W_UK), latent attention with split-KV, combine, and the
-value out-projection (W_UV).  Buffers are allocated once, at construction."""
+value out-projection (W_UV).  Buffers are allocated once, at construction;
+a step over fixed input buffers can be recorded once as a CUDA graph and
+replayed, which removes the host launch overhead of the four calls."""
 from __future__ import annotations
 
 import torch
@@ -30,6 +32,24 @@ class MLADecodeStep:
                      self.workspace, self.o_lat, self.lse, stream)
         L.mla_split_kv_combine(p, self.workspace, G, self.o_lat, self.lse, stream)
         L.mla_out_proj(p, self.o_lat, w_uv, self.out, stream)
+        return self.out
+
+    def capture(self, *inputs):
+        """Record one step over these input buffers (the arguments of
+        __call__, which must stay allocated and at the same addresses) as a
+        CUDA graph; replay() then runs it on the current stream."""
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            self(*inputs)  # warm-up outside the capture (first-call set-up)
+        torch.cuda.current_stream().wait_stream(side)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self(*inputs)
+        return self.graph
+
+    def replay(self):
+        self.graph.replay()
         return self.out
 
     def status(self, clear=False):
