@@ -6,11 +6,14 @@
 // splitting with its 128K contexts): for the partials s of one (sequence,
 // head), o = sum_s exp(lse_s - L) O_s with L = log sum_s exp(lse_s), each O_s
 // normalised over its own range.
-#include "common.cuh"
 #include "kernels.h"
+#include "tc.cuh"
+#include "tmap.cuh"
 
 namespace mla {
 namespace {
+
+using namespace tc;
 
 // One CTA per (sequence, head) of a split sequence; thread t owns latent
 // columns [4t, 4t+4).  The partials of the sequence are the records of the
@@ -24,24 +27,44 @@ __global__ void __launch_bounds__(128) combine_kernel(const __nv_bfloat16* __res
   __shared__ int s_slot[128];
   __shared__ float s_val[128];
   __shared__ float s_red[4];
+  grid_dep_wait();  // the decode kernel's partials
+  grid_dep_trigger();
   const int b = blockIdx.x, h = blockIdx.y, t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  __shared__ int s_wf, s_n;
+  __shared__ long long s_sb;
+  if (t == 0) {  // the workers holding this sequence's pages (one thread: 64-bit divisions)
+    const long long P = seq_start[B];
+    const long long sb = seq_start[b], se = seq_start[b + 1];
+    int wf = 0, n = 0;
+    if (se > sb) {
+      wf = worker_of(sb, G, P);
+      n = worker_of(se - 1, G, P) - wf + 1;
+    }
+    s_wf = wf;
+    s_n = n;
+    s_sb = sb;
+  }
+  __syncthreads();
+  const int wf = s_wf, n = s_n;
+  const long long sb = s_sb;
+  if (n <= 1) return;  // empty, or finished by the decode kernel
   const long long P = seq_start[B];
-  const long long sb = seq_start[b], se = seq_start[b + 1];
-  if (se <= sb) return;
-  const int wf = worker_of(sb, G, P), wl = worker_of(se - 1, G, P);
-  if (wf == wl) return;  // finished by the decode kernel
-  const int n = wl - wf + 1;
   // slot of partial i, or -1 for an empty worker range (no partial written)
   auto slot_of = [&](int i) {
     const int w = wf + i;
     const long long lo = range_lo(w, G, P), hi = range_lo(w + 1, G, P);
     return lo == hi ? -1 : (sb <= lo ? w : G + w);
   };
-  // pass 1: the largest partial log-sum-exp
+  // pass 1: the largest partial log-sum-exp (slots kept when they all fit)
   float mx = -INFINITY;
   for (int i = t; i < n; i += 128) {
     const int sl = slot_of(i);
-    if (sl >= 0) mx = fmaxf(mx, part_lse[(size_t)sl * H + h]);
+    const float l = sl >= 0 ? part_lse[(size_t)sl * H + h] : -INFINITY;
+    mx = fmaxf(mx, l);
+    if (n <= 128) {
+      s_slot[i] = sl;
+      s_val[i] = l;
+    }
   }
 #pragma unroll
   for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
@@ -55,8 +78,15 @@ __global__ void __launch_bounds__(128) combine_kernel(const __nv_bfloat16* __res
     const int m = min(128, n - c0);
     __syncthreads();  // the previous chunk's entries are no longer read
     if (t < m) {
-      const int sl = slot_of(c0 + t);
-      const float l = sl >= 0 ? part_lse[(size_t)sl * H + h] : -INFINITY;
+      int sl;
+      float l;
+      if (n <= 128) {
+        sl = s_slot[t];
+        l = s_val[t];
+      } else {
+        sl = slot_of(c0 + t);
+        l = sl >= 0 ? part_lse[(size_t)sl * H + h] : -INFINITY;
+      }
       s_slot[t] = sl;
       s_val[t] = l == -INFINITY ? 0.f : __expf(l - mx);
     }
@@ -86,8 +116,8 @@ __global__ void __launch_bounds__(128) combine_kernel(const __nv_bfloat16* __res
 cudaError_t launch_combine(const __nv_bfloat16* part_o, const float* part_lse, const int* seq_start,
                            __nv_bfloat16* o_lat, float* lse, int B, int H, int G, cudaStream_t stream) {
   dim3 grid(B, H);
-  combine_kernel<<<grid, 128, 0, stream>>>(part_o, part_lse, seq_start, o_lat, lse, B, H, G);
-  return cudaGetLastError();
+  return launch_dependent(combine_kernel, grid, dim3(128), 0, stream, part_o, part_lse, seq_start, o_lat, lse, B,
+                          H, G);
 }
 
 }  // namespace mla

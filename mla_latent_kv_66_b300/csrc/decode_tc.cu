@@ -208,6 +208,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   __shared__ uint16_t mx_swap[2][2][128];  // row maxima between the two softmax warpgroups
   __shared__ int page_ids[kIdRing];        // producer-private
 
+  // launched as a dependent of the previous kernel on the stream: nothing is
+  // read before that kernel has finished; the combine may launch right away
+  grid_dep_wait();
+  grid_dep_trigger();
   const uint32_t rank = cluster_rank(), peer = rank ^ 1u;
   const int w = blockIdx.x >> 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -919,8 +923,7 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t stream) {
   const uint32_t smem = fp8 ? Layout<true>::kSmemBytes : Layout<false>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kernel<<<2 * a.G, kThreads, smem, stream>>>(tc_map, tk_map, a);
-  return cudaGetLastError();
+  return launch_dependent(kernel, dim3(2 * a.G), dim3(kThreads), smem, stream, tc_map, tk_map, a);
 }
 
 }  // namespace mla

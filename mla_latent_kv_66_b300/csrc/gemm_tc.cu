@@ -23,6 +23,7 @@ constexpr uint32_t kABytes = 16384;  // A bytes per 64-wide K block
 
 struct GemmTcArgs {
   int B, H, N;
+  const __nv_bfloat16* weight;  // [H,128,512]: prefetched into L2 before the dependency wait
   void* out;
   int out_kind;  // 0: q_lat bf16 [B,H,512]; 1: out fp32 [B,H,128]; 2: out bf16 [B,H,128]
 };
@@ -46,6 +47,13 @@ __global__ void __launch_bounds__(128, 1)
   const uint32_t full = smem_u32(&bars[0]), empty = smem_u32(&bars[S]), done = smem_u32(&bars[2 * S]);
   const uint32_t ncols = g.N <= 32 ? 32 : g.N <= 64 ? 64 : g.N <= 128 ? 128 : 256;
 
+  // q absorption opens a decode step: the decode kernel may launch at once.
+  // The out-projection follows the combine: its weight slice (independent of
+  // the combine) is pulled into L2 while the combine runs.
+  if (kMode == 0) grid_dep_trigger();
+  if (kMode == 1 && threadIdx.x == 32 && mt == 0 && nt == 0)
+    prefetch_l2(g.weight + (size_t)h * kV * kLatent, kV * kLatent * 2);
+  grid_dep_wait();
   if (threadIdx.x == 0) {
     abort_flag = 0;
     for (int i = 0; i < S; ++i) {
@@ -163,7 +171,7 @@ cudaError_t launch_absorb_tc(const __nv_bfloat16* q_nope, const __nv_bfloat16* w
   if (!make_tmap(&tA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w_uk, ad, as, abox) ||
       !make_tmap(&tB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q_nope, bd, bs, bbox))
     return cudaErrorInvalidValue;
-  GemmTcArgs g{B, H, N, q_lat, 0};
+  GemmTcArgs g{B, H, N, w_uk, q_lat, 0};
   const size_t smem = 2 * (kABytes + (size_t)N * 128) + 1024;
   cudaFuncSetAttribute(gemm_tc_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   dim3 grid(H, kLatent / 128, (B + N - 1) / N);
@@ -184,12 +192,11 @@ cudaError_t launch_out_proj_tc(const __nv_bfloat16* o_lat, const __nv_bfloat16* 
   if (!make_tmap(&tA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w_uv, ad, as, abox) ||
       !make_tmap(&tB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, o_lat, bd, bs, bbox))
     return cudaErrorInvalidValue;
-  GemmTcArgs g{B, H, N, out, out_bf16 ? 2 : 1};
+  GemmTcArgs g{B, H, N, w_uv, out, out_bf16 ? 2 : 1};
   const size_t smem = 4 * (kABytes + (size_t)N * 128) + 1024;
   cudaFuncSetAttribute(gemm_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   dim3 grid(H, 1, (B + N - 1) / N);
-  gemm_tc_kernel<1><<<grid, 128, smem, stream>>>(tA, tB, g);
-  return cudaGetLastError();
+  return launch_dependent(gemm_tc_kernel<1>, grid, dim3(128), smem, stream, tA, tB, g);
 }
 
 }  // namespace mla

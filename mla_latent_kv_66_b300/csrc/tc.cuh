@@ -145,6 +145,15 @@ __device__ inline void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// ---------------------------------------------------------------- dependent launch
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start before the preceding kernel on its stream has
+// finished; grid_dep_wait blocks until that kernel has completed and its
+// memory is visible, and grid_dep_trigger lets the following kernel launch
+// early.  Both are no-ops for a launch without that attribute.
+__device__ inline void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ inline void grid_dep_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- tcgen05
 __device__ inline void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
