@@ -13,11 +13,10 @@
 // score over its part (rank 1 adds the shared RoPE key).  The two partial
 // score tiles are swapped through distributed shared memory in the log2
 // domain as fp16 (half the bytes of fp32; the SM-to-SM network, not HBM, is
-// the scarce resource here) and each CTA adds its own fp32 partial to the
-// peer's fp16 one.  The two CTAs' scores therefore differ by the fp16
-// rounding of one partial (2^-11 relative), so each CTA normalises its half
-// of O with its own row sum; rank 0's log-sum-exp is the one reported.  Each
-// CTA then accumulates P . c over its own 256 latent columns.
+// the scarce resource here); each CTA adds its own staged fp16 partial to
+// the peer's, so both see the same scores and take the same softmax
+// decisions.  Each CTA then accumulates P . c over its own 256 latent
+// columns.
 //
 // Warp roles (512 threads):
 //   warp 0       TMA producer (cache pages, 3-stage ring, L2 prefetch ahead)
@@ -26,16 +25,18 @@
 //                consumed" to the peer CTA and re-arms the receive barrier
 //   warp 3       KV-partition schedule, split records; then MMA issuer for
 //                O += P V (a separate issuer lets S = Q K^T run ahead)
-//   warps 4..7   exchange: stage each partial score tile (fp16) in shared
-//                memory as soon as its S = Q K^T completes and send it to the
-//                peer CTA with one bulk copy; double-buffered
+//   warps 4..7   exchange: copy each partial score tile out of tensor memory
+//                as soon as its S = Q K^T completes (S has one buffer), stage
+//                it as fp16 in shared memory and send it to the peer CTA with
+//                one bulk copy; double-buffered
 //   warps 8..15  two softmax warpgroups; warpgroup j owns tokens [32j, 32j+32)
-//                of every page, thread = head row: own fp32 partial + the
-//                peer's fp16 partial, row maximum agreed with the other
-//                warpgroup, online softmax with lazy rescaling, its half of P
-//                to shared memory, its half of O rescaled when needed and
-//                written at the end of a unit.
-// Tensor memory: O [0,256), S double buffer [256,384), query [384,512).
+//                of every page, thread = head row: own staged fp16 partial +
+//                the peer's, row maximum agreed with the other warpgroup,
+//                online softmax with lazy rescaling, its half of P into tensor
+//                memory (two P buffers), its half of O rescaled when needed
+//                and written at the end of a unit.
+// Tensor memory: O [0,256), S [256,320), P double buffer [320,384) (bf16
+// pairs, the A operand of P . V), query [384,512).
 #include <cuda_fp16.h>
 
 #include "kernels.h"
@@ -64,12 +65,11 @@ struct Layout {
   static constexpr uint32_t kStageBytes = kFp8 ? kStageBf + 1024 : kStageBf;
   static constexpr uint32_t kOffRaw = kStages * kStageBytes;
   static constexpr uint32_t kOffQpe = kOffRaw + kRaw * kRawBytes;  // [128 x 64] bf16 (rank 1)
-  static constexpr uint32_t kOffP = kOffQpe + 16384;               // [128 x 64] bf16 probabilities
-  static constexpr uint32_t kOffX = kOffP + 16384;                 // 2 x peer partial scores
+  static constexpr uint32_t kOffX = kOffQpe + 16384;               // 2 x peer partial scores
   static constexpr uint32_t kOffXs = kOffX + 2 * kXBytes;          // 2 x own partial, outgoing
   static constexpr uint32_t kSmemBytes = kOffXs + 2 * kXBytes + 1024;
 };
-constexpr uint32_t kTmO = 0, kTmS = 256, kTmQ = 384;
+constexpr uint32_t kTmO = 0, kTmS = 256, kTmP = 320, kTmQ = 384;
 constexpr int kThreads = 512;
 constexpr float kRescaleLog2 = 8.f;  // lazy rescale threshold: P stays <= 2^8
 constexpr int kPrefetchPages = 6;    // L2 prefetch distance of the producer, in pages
@@ -85,9 +85,9 @@ enum {
   B_XFULL = B_SFREE + 2,
   B_XFREE = B_XFULL + 2,
   B_XREAD = B_XFREE + 2,
-  B_PFULL = B_XREAD + 2,
-  B_PFREE,
-  B_ODONE,
+  B_PFULL = B_XREAD + 2,            // P buffer i written (tensor memory)
+  B_PVD = B_PFULL + 2,              // the P . V that read P buffer i is done
+  B_ODONE = B_PVD + 2,
   B_OFREE,
   B_QFULL,
   B_QFREE,
@@ -198,7 +198,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   using L = Layout<kFp8>;
   constexpr int kStages = L::kStages;
   constexpr uint32_t kStageBytes = L::kStageBytes;
-  constexpr uint32_t kOffQpe = L::kOffQpe, kOffP = L::kOffP, kOffX = L::kOffX, kOffXs = L::kOffXs;
+  constexpr uint32_t kOffQpe = L::kOffQpe, kOffX = L::kOffX, kOffXs = L::kOffXs;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bars[B_COUNT];
   __shared__ uint32_t tmem_slot;
@@ -206,6 +206,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   __shared__ long long sh_P, sh_s0;
   __shared__ int sh_b0;
   __shared__ uint16_t mx_swap[2][2][128];  // row maxima between the two softmax warpgroups
+  __shared__ uint32_t lsum_swap[2 * 128];  // row sums between them at the end of a unit
   __shared__ int page_ids[kIdRing];        // producer-private
 
   // launched as a dependent of the previous kernel on the stream: nothing is
@@ -228,15 +229,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(bar(B_RFULL + i), 1);
       mbar_init(bar(B_RFREE + i), 128);
     }
+    mbar_init(bar(B_SFULL), 1);
+    mbar_init(bar(B_SFREE), 128);  // the exchange warps have read S
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(B_SFULL + i), 1);
-      mbar_init(bar(B_SFREE + i), 384);  // exchange + both softmax warpgroups
       mbar_init(bar(B_XFULL + i), 1);    // local arm + 16 KB of the peer's st.async
       mbar_init(bar(B_XFREE + i), 1);    // the peer's relay: its buffer is consumed
       mbar_init(bar(B_XREAD + i), 256);  // local softmax threads consumed buffer i
     }
-    mbar_init(bar(B_PFULL), 256);
-    mbar_init(bar(B_PFREE), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(B_PFULL + i), 256);
+      mbar_init(bar(B_PVD + i), 1);
+    }
     mbar_init(bar(B_ODONE), 1);
     mbar_init(bar(B_OFREE), 256);
     mbar_init(bar(B_QFULL), 256);
@@ -406,14 +409,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (!mbar_wait(bar(B_QFULL), uc & 1, &abort_flag, a.err)) break;
         tc_fence_after();
         for (int i = 0; i < np; ++i) {
-          const uint32_t gi = g + i, s = gi % kStages, sb = gi & 1;
+          const uint32_t gi = g + i, s = gi % kStages;
+          // S has one buffer: the exchange warps copy it out as soon as it is done
           if (!mbar_wait(bar(B_FULL + s), (gi / kStages) & 1, &abort_flag, a.err) ||
-              (gi >= 2 && !mbar_wait(bar(B_SFREE + sb), ((gi >> 1) - 1) & 1, &abort_flag, a.err))) {
+              (gi >= 1 && !mbar_wait(bar(B_SFREE), (gi - 1) & 1, &abort_flag, a.err))) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t st = base + s * kStageBytes, d = tmem + kTmS + sb * 64;
+          const uint32_t st = base + s * kStageBytes, d = tmem + kTmS;
 #pragma unroll
           for (int kk = 0; kk < 16; ++kk)
             mma_bf16_ts(d, tmem + kTmQ + kk * 8,
@@ -425,7 +429,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               mma_bf16_ss(d, sdesc_sw128(base + kOffQpe + kk * 32, 16, 1024),
                           sdesc_sw128(st + 4 * kBox + kk * 32, 16, 1024), idesc_qk, 1u);
           }
-          mma_commit(bar(B_SFULL + sb));
+          mma_commit(bar(B_SFULL));
           if (i == np - 1) mma_commit(bar(B_QFREE));
         }
         g += np;
@@ -476,20 +480,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       while (ok && wk.next(a, u)) {
         const int np = u.pe - u.pb;
         for (int i = 0; i < np; ++i) {
-          const uint32_t gp = g + i, s = gp % kStages;
-          if (!mbar_wait(bar(B_PFULL), gp & 1, &abort_flag, a.err) ||
+          const uint32_t gp = g + i, s = gp % kStages, pb = gp & 1;
+          if (!mbar_wait(bar(B_PFULL + pb), (gp >> 1) & 1, &abort_flag, a.err) ||
               (i == 0 && uc >= 1 && !mbar_wait(bar(B_OFREE), (uc - 1) & 1, &abort_flag, a.err))) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t st = base + s * kStageBytes;
+          // A = P from tensor memory (two bf16 per column), B = the stage's latent
+          const uint64_t cdesc = sdesc_sw128(base + s * kStageBytes, kBox, 1024);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_bf16_ss(tmem + kTmO, sdesc_sw128(base + kOffP + kk * 32, 16, 1024),
-                        sdesc_sw128(st + kk * 2048, kBox, 1024), idesc_pv,
+            mma_bf16_ts(tmem + kTmO, tmem + kTmP + pb * 32 + kk * 8, cdesc + kk * 128, idesc_pv,
                         (i > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(bar(B_PFREE));
+          mma_commit(bar(B_PVD + pb));
           mma_commit(bar(B_EMPTY + s));
           if (i == np - 1) mma_commit(bar(B_ODONE));
         }
@@ -566,23 +570,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     while (ok && wk.next(a, u)) {
       for (int jp = u.pb; jp < u.pe; ++jp, ++g) {
         const uint32_t sb = g & 1;
-        if (!wwait(B_SFULL + sb, (g >> 1) & 1)) { ok = false; break; }
+        if (!wwait(B_SFULL, g & 1)) { ok = false; break; }
         tc_fence_after();
         uint32_t hx[32];
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           uint32_t s32[32];
-          tmem_ld32(tmem + lane_base + kTmS + sb * 64 + half * 32, s32);
+          tmem_ld32(tmem + lane_base + kTmS + half * 32, s32);
           tmem_wait_ld();
 #pragma unroll
           for (int k = 0; k < 16; ++k)
             hx[half * 16 + k] = pack_h2(__uint_as_float(s32[2 * k]) * c, __uint_as_float(s32[2 * k + 1]) * c);
         }
         tc_fence_before();
-        mbar_arrive(bar(B_SFREE + sb));
+        mbar_arrive(bar(B_SFREE));
         // staging buffer sb and the peer's buffer sb are free once the peer has
-        // consumed page g-2 (its copy has then finished reading ours)
-        if (g >= 2 && !wwait_c(B_XFREE + sb, ((g >> 1) - 1) & 1)) { ok = false; break; }
+        // consumed page g-2 (its copy has then finished reading ours) and our
+        // own softmax warps have read page g-2 from staging
+        if (g >= 2 && (!wwait_c(B_XFREE + sb, ((g >> 1) - 1) & 1) || !wwait(B_XREAD + sb, ((g >> 1) - 1) & 1))) {
+          ok = false;
+          break;
+        }
         const uint32_t stg = base + kOffXs + sb * kXBytes;
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc)
@@ -608,11 +616,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int j = (warp - 8) >> 2;
     const int h = (warp & 3) * 32 + lane;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const float c = a.scale_log2;
     const int H = a.H;
-    // the P buffer doubles as the exchange area of the row sums at the end of a
-    // unit, when no P . V is pending
-    uint32_t* const lsum_swap = reinterpret_cast<uint32_t*>(smem_raw + (base + kOffP - smem_u32(smem_raw)));
     uint32_t xk = 0;  // phases of the warpgroup-exchange barrier consumed
 
     // Swap one value per row with the other warpgroup (bounded wait).  Row
@@ -696,27 +700,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int valid = page_ok ? min(kPage, u.n - jp * kPage) : 0;
         if (!page_ok && h == 0 && j == 0 && rank == 0) set_error(a.err, MLA_ERR_PAGE_OOB);
 
-        // own partial score (fp32) plus the peer's (fp16), in the log2 domain
-        if (!wwait(B_SFULL + sb, (gi >> 1) & 1)) { ok = false; break; }
-        tc_fence_after();
-        uint32_t s32[32];
-        tmem_ld32(tmem + lane_base + kTmS + sb * 64 + j * 32, s32);
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(bar(B_SFREE + sb));
-        if (!wwait_c(B_XFULL + sb, (gi >> 1) & 1)) { ok = false; break; }
+        // score in the log2 domain: own partial (staged by the exchange warps)
+        // plus the peer's, both fp16; both CTAs add the same two numbers
+        if (!wwait_c(B_XFULL + sb, (gi >> 1) & 1) || !wwait(B_XSTAGED + sb, (gi >> 1) & 1)) {
+          ok = false;
+          break;
+        }
         float x[32];
-        const uint32_t xbuf = base + kOffX + sb * kXBytes;
+        const uint32_t xbuf = base + kOffX + sb * kXBytes, obuf = base + kOffXs + sb * kXBytes;
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
           const uint4 v = ld_shared_v4u(xbuf + x_off(h, 4 * j + cc));
-          const uint32_t pv[4] = {v.x, v.y, v.z, v.w};
+          const uint4 o = ld_shared_v4u(obuf + x_off(h, 4 * j + cc));
+          const uint32_t pv[4] = {v.x, v.y, v.z, v.w}, ov[4] = {o.x, o.y, o.z, o.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float2 b2 = unpack_h2(pv[e]);
+            const float2 b2 = unpack_h2(pv[e]), a2 = unpack_h2(ov[e]);
             const int k = 8 * cc + 2 * e;
-            x[k] = fmaf(__uint_as_float(s32[k]), c, b2.x);
-            x[k + 1] = fmaf(__uint_as_float(s32[k + 1]), c, b2.y);
+            x[k] = a2.x + b2.x;
+            x[k + 1] = a2.y + b2.y;
           }
         }
         mbar_arrive(bar(B_XREAD + sb));  // relayed to the peer by warp 2
@@ -789,10 +791,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
 
-        // P buffer and O are free once the previous page's P V has finished
-        if (gi >= 1 && !wwait(B_PFREE, (gi - 1) & 1)) { ok = false; break; }
+        // P buffer gi&1 (tensor memory) is free once the P . V of page gi-2 has
+        // finished; O may be rescaled only after the P . V of page gi-1
+        const uint32_t pb = gi & 1;
+        if (gi >= 2 && !wwait(B_PVD + pb, ((gi >> 1) - 1) & 1)) { ok = false; break; }
+        const bool any_resc = __any_sync(0xffffffffu, resc);
+        if (any_resc && !wwait(B_PVD + (pb ^ 1), ((gi - 1) >> 1) & 1)) { ok = false; break; }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, resc)) {  // this warpgroup's 128 O columns
+        if (any_resc) {  // this warpgroup's 128 O columns
           const float f = resc ? alpha : 1.f;
 #pragma unroll 1
           for (int cc = 0; cc < 4; ++cc) {
@@ -806,13 +812,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           tmem_wait_st();
         }
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
-          st_shared_v4(base + kOffP + h * 128 + (((4 * j + cc) ^ (h & 7)) * 16), pk[4 * cc],
-                       pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-        fence_proxy_async_smem();
+        // this warpgroup's 32 tokens of P: 16 tensor-memory columns of bf16 pairs
+        tmem_st16(tmem + lane_base + kTmP + pb * 32 + j * 16, pk);
+        tmem_wait_st();
+        fence_proxy_async_smem();  // the zeroed stage rows above
         tc_fence_before();
-        mbar_arrive(bar(B_PFULL));
+        mbar_arrive(bar(B_PFULL + pb));
       }
       if (!ok) break;
 
