@@ -19,7 +19,7 @@
 // columns.
 //
 // Warp roles (512 threads):
-//   warp 0       TMA producer (cache pages, 3-stage ring, L2 prefetch ahead)
+//   warp 0       TMA producer (cache pages, 3-stage ring)
 //   warp 1       MMA issuer for S = Q K^T (A = query in tensor memory)
 //   warp 2       tensor-memory allocation; then relays "exchange buffer
 //                consumed" to the peer CTA and re-arms the receive barrier
@@ -72,8 +72,7 @@ struct Layout {
 constexpr uint32_t kTmO = 0, kTmS = 256, kTmP = 320, kTmQ = 384;
 constexpr int kThreads = 512;
 constexpr float kRescaleLog2 = 8.f;  // lazy rescale threshold: P stays <= 2^8
-constexpr int kPrefetchPages = 6;    // L2 prefetch distance of the producer, in pages
-constexpr int kIdRing = 16;          // page ids copied ahead by the producer (> kPrefetchPages)
+constexpr int kIdRing = 16;          // page ids read ahead by the producer
 
 enum {
   B_FULL = 0,                       // bf16 stage ready (TMA landed, or E4M3 expanded)
@@ -340,21 +339,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int pg = page_ids[k % kIdRing];
         return pg >= 0 && pg < a.num_pages ? pg : -1;
       };
-      // L2 prefetch runs kPrefetchPages pages ahead of the TMA ring, so the
-      // ring's loads hit L2; rank 0 fetches the whole latent page, rank 1
-      // the rope page (and, for E4M3, the scales).
-      auto prefetch_page = [&](int page) {
-        if (page < 0) return;
-        constexpr uint32_t es = kFp8 ? 1 : 2;  // bytes per cached value
-        if (rank == 0)
-          prefetch_l2(static_cast<const uint8_t*>(a.ckv) + (size_t)page * kPage * kLatent * es,
-                      kPage * kLatent * es);
-        else
-          prefetch_l2(static_cast<const uint8_t*>(a.kpe) + (size_t)page * kPage * kRope * es,
-                      kPage * kRope * es);
-        if (kFp8 && rank == 1) prefetch_l2(a.kv_scale + (size_t)page * kPage, kPage * 4);
-      };
-      for (uint32_t k = 0; k < (uint32_t)kPrefetchPages && k < npages; ++k) prefetch_page(page_at(k));
       // bf16: pages go straight into the stage ring.  E4M3: pages go into the
       // raw ring (codes and scales) and the exchange warps expand them.
       constexpr int kRing = kFp8 ? L::kRaw : kStages;
@@ -385,8 +369,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               tma_load_2d(st + i * kBox, &tm_ckv, fb, (int)rank * 256 + i * 64, page * kPage);
             if (rank == 1) tma_load_2d(st + 4 * kBox, &tm_kpe, fb, 0, page * kPage);
           }
-          // keep the L2 prefetch kPrefetchPages and the page ids kIdRing ahead
-          if (g + kPrefetchPages < npages) prefetch_page(page_at(g + kPrefetchPages));
+          // keep the page ids kIdRing ahead.  (An L2 prefetch of the pages ahead
+          // of the ring was measured to slow the stream down: the TMA loads
+          // alone keep enough bytes in flight.)
           id_fetch();  // stores the id of page g + kIdRing - 1, loads the next one
         }
       }
@@ -418,16 +403,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const uint32_t st = base + s * kStageBytes, d = tmem + kTmS;
+          // one descriptor per operand and page; K-step kk is a constant offset
+          // (16-byte units) into it, so the MMAs issue back to back
+          const uint64_t kdesc = sdesc_sw128(st, 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < 16; ++kk)
-            mma_bf16_ts(d, tmem + kTmQ + kk * 8,
-                        sdesc_sw128(st + (kk >> 2) * kBox + (kk & 3) * 32, 16, 1024), idesc_qk,
-                        kk > 0 ? 1u : 0u);
+            mma_bf16_ts(d, tmem + kTmQ + kk * 8, kdesc + (uint64_t)(((kk >> 2) * kBox + (kk & 3) * 32) >> 4),
+                        idesc_qk, kk > 0 ? 1u : 0u);
           if (rank == 1) {
+            const uint64_t qdesc = sdesc_sw128(base + kOffQpe, 16, 1024);
+            const uint64_t rdesc = sdesc_sw128(st + 4 * kBox, 16, 1024);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_bf16_ss(d, sdesc_sw128(base + kOffQpe + kk * 32, 16, 1024),
-                          sdesc_sw128(st + 4 * kBox + kk * 32, 16, 1024), idesc_qk, 1u);
+            for (int kk = 0; kk < 4; ++kk) mma_bf16_ss(d, qdesc + kk * 2, rdesc + kk * 2, idesc_qk, 1u);
           }
           mma_commit(bar(B_SFULL));
           if (i == np - 1) mma_commit(bar(B_QFREE));
