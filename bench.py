@@ -51,6 +51,12 @@ def peaks():
     return 6400.0, 1800.0, "fallback"
 
 
+# DRAM bytes (read + write) of one decode launch, from one ncu capture of the
+# kernel as committed (profiles/decode_tc_v2_layer.md, decode_tc_fp8_batch.md);
+# None for workloads not captured.
+NCU_TRAFFIC_BYTES = {"v2_layer": 162.69e6, "fp8_batch": 655.14e6}
+
+
 def cache_bytes_per_token(kv_dtype):
     return 576 * 2 if kv_dtype == "bf16" else 576 + 4
 
@@ -342,6 +348,7 @@ def main():
     cfg = {"workload": w.name, "B": w.B, "H": w.H, "L": w.L or "log-uniform[%d,%d]" % w.ragged,
            "kv_lora_rank": 512, "rope_dim": 64, "page_size": 64, "kv_dtype": w.kv_dtype,
            "pages": w.pages, "l2": "flushed before every timed step (256 MiB write)",
+           "step": "CUDA graph: q absorption, decode, split-KV combine, out-projection",
            "parallelism": "replicas" if world > 1 else "single-gpu"}
     if args.impl == "reference":
         if rank != 0:
@@ -372,6 +379,17 @@ def main():
     value = world * tokens_per_step / (r["ms"] / 1000.0)
     cache_bytes = r["tokens"] * cache_bytes_per_token(w.kv_dtype)
     achieved = cache_bytes / (r["dec_ms"] / 1000.0) / 1e9
+    if w.kv_dtype == "bf16":
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm}
+    else:
+        # E4M3 cache: 2*H*(576+512) flops per cached token over 580 bytes, above
+        # the ridge, so the bound is the bf16 tensor rate (the MMAs run in bf16)
+        flops = r["tokens"] * 2.0 * w.H * (576 + 512)
+        tf = flops / (r["dec_ms"] / 1000.0) / 1e12
+        roofline = {"bound": "tensor", "achieved": tf, "peak": tflops, "unit": "TFLOP/s", "frac": tf / tflops,
+                    "cache_gbs": achieved, "cache_frac_of_hbm": achieved / hbm}
+    roofline.update({"traffic": NCU_TRAFFIC_BYTES.get(w.name), "kernel": "mla_decode", "peak_source": src,
+                     "decode_ms": r["dec_ms"]})
     cpu = None
     if not args.no_cpu_baseline:
         v, cores, desc = cpu_oracle_sample(w)
@@ -383,9 +401,7 @@ def main():
         "data": "synthetic (seeded, DeepSeek-V2 MLA shapes; random-init weights)", "config": cfg,
         "cache_gbs": achieved, "cache_bytes_per_step": cache_bytes,
         "cached_tokens_per_s": r["tokens"] / (r["dec_ms"] / 1000.0),
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": None, "kernel": "mla_decode",
-                     "peak_source": src, "decode_ms": r["dec_ms"]},
+        "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": {"value": world * tokens_per_step / (r["e2e_ms"] / 1000.0), "unit": "tokens/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
