@@ -7,10 +7,12 @@
 // shared by all heads.
 //
 // The fp32 latent accumulator O[128 heads x 512] alone needs all 512 tensor
-// memory columns of an SM, so a cluster of two CTAs splits the latent axis:
-//   rank 0: latent columns [0,256);  rank 1: latent [256,512) and k_pe.
-// Each CTA TMA-loads only its part of every page and computes the partial
-// score over its part (rank 1 adds the shared RoPE key).  The two partial
+// memory columns of an SM, so a cluster of two CTAs splits the latent axis
+// and the shared RoPE key evenly:
+//   rank 0: latent columns [0,256), k_pe [0,32);
+//   rank 1: latent columns [256,512), k_pe [32,64).
+// Each CTA TMA-loads only its part of every page (36 KB of the 72 KB) and
+// computes the partial score over its 288 of the 576 dimensions.  The two partial
 // score tiles are swapped through distributed shared memory in the log2
 // domain as fp16 (half the bytes of fp32; the SM-to-SM network, not HBM, is
 // the scarce resource here); each CTA adds its own staged fp16 partial to
@@ -19,16 +21,17 @@
 // columns.
 //
 // Warp roles (512 threads):
-//   warp 0       TMA producer (cache pages, 3-stage ring)
+//   warp 0       TMA producer (cache pages, 4-stage ring)
 //   warp 1       MMA issuer for S = Q K^T (A = query in tensor memory)
 //   warp 2       tensor-memory allocation; then relays "exchange buffer
 //                consumed" to the peer CTA and re-arms the receive barrier
-//   warp 3       KV-partition schedule, split records; then MMA issuer for
+//   warp 3       KV-partition schedule, the first page ids of the range,
+//                split records; then MMA issuer for
 //                O += P V (a separate issuer lets S = Q K^T run ahead)
 //   warps 4..7   exchange: copy each partial score tile out of tensor memory
 //                as soon as its S = Q K^T completes (S has one buffer), stage
 //                it as fp16 in shared memory and send it to the peer CTA with
-//                one bulk copy; double-buffered
+//                one bulk copy per warp; double-buffered
 //   warps 8..15  two softmax warpgroups; warpgroup j owns tokens [32j, 32j+32)
 //                of every page, thread = head row: own staged fp16 partial +
 //                the peer's, row maximum agreed with the other warpgroup,
@@ -49,30 +52,35 @@ namespace {
 using namespace tc;
 
 constexpr uint32_t kBox = 8192;            // [64 rows x 64 bf16], 128-byte swizzle
-constexpr uint32_t kStageBf = 5 * kBox;    // bf16 stage: 4 latent boxes + k_pe box (rank 1)
+constexpr uint32_t kKpeBox = 4096;         // [64 rows x 32 bf16], 64-byte swizzle
+constexpr uint32_t kStageBf = 4 * kBox + kKpeBox;  // bf16 stage: 4 latent boxes + this CTA's k_pe half
 constexpr uint32_t kXBytes = 16384;        // [128 x 64] fp16 partial-score tile
 // E4M3 cache: a raw page holds this CTA's 256 latent codes of 64 tokens as two
-// [64 x 128 B] boxes, the 64 rope codes (rank 1, [64 x 64 B]) and the page's
-// 64 fp32 scales; after expansion the bf16 stage also carries the scales.
-constexpr uint32_t kRawKpe = 2 * 8192, kRawScale = kRawKpe + 4096, kRawBytes = 21504;
+// [64 x 128 B] boxes, its 32 rope codes ([64 x 32 B]) and the page's 64 fp32
+// scales; after expansion the bf16 stage also carries the scales.
+constexpr uint32_t kRawKpe = 2 * 8192, kRawScale = kRawKpe + 2048, kRawBytes = kRawScale + 256;
 constexpr uint32_t kStageScale = kStageBf;
-constexpr int kMaxStages = 3;
+constexpr int kMaxStages = 4;
 
 template <bool kFp8>
 struct Layout {
-  static constexpr int kStages = kFp8 ? 2 : 3;   // bf16 stages the MMAs read
+  static constexpr int kStages = kFp8 ? 2 : 4;   // bf16 stages the MMAs read
   static constexpr int kRaw = kFp8 ? 2 : 0;      // raw E4M3 pages
   static constexpr uint32_t kStageBytes = kFp8 ? kStageBf + 1024 : kStageBf;
   static constexpr uint32_t kOffRaw = kStages * kStageBytes;
-  static constexpr uint32_t kOffQpe = kOffRaw + kRaw * kRawBytes;  // [128 x 64] bf16 (rank 1)
-  static constexpr uint32_t kOffX = kOffQpe + 16384;               // 2 x peer partial scores
+  static constexpr uint32_t kOffQpe = kOffRaw + kRaw * kRawBytes;  // [128 x 32] bf16, 64-byte swizzle
+  static constexpr uint32_t kOffX = kOffQpe + 8192;                // 2 x peer partial scores
   static constexpr uint32_t kOffXs = kOffX + 2 * kXBytes;          // 2 x own partial, outgoing
   static constexpr uint32_t kSmemBytes = kOffXs + 2 * kXBytes + 1024;
+  static_assert(kStageBytes % 1024 == 0 && kRawBytes % 128 == 0 && kOffQpe % 512 == 0,
+                "swizzled tiles need 1024-byte (128 B swizzle) / 512-byte (64 B) alignment");
+  static_assert(kSmemBytes + 4096 <= 232448, "shared memory per CTA");
 };
 constexpr uint32_t kTmO = 0, kTmS = 256, kTmP = 320, kTmQ = 384;
 constexpr int kThreads = 512;
 constexpr float kRescaleLog2 = 8.f;  // lazy rescale threshold: P stays <= 2^8
 constexpr int kIdRing = 16;          // page ids read ahead by the producer
+constexpr int kTouch = 4;            // start-up touches: pages 32, 64, ... of the range and its last
 
 enum {
   B_FULL = 0,                       // bf16 stage ready (TMA landed, or E4M3 expanded)
@@ -92,6 +100,7 @@ enum {
   B_QFREE,
   B_IDLE,
   B_MX,
+  B_TOUCH,                          // start-up touches of the range's later memory pages landed
   B_XSTAGED,
   B_COUNT = B_XSTAGED + 2
 };
@@ -101,14 +110,17 @@ struct Unit {
   bool split, at_lo, at_hi;
 };
 
-// Walks the units of one worker range [lo, hi) of flattened pages.
+// Walks the units of one worker range [lo, hi) of flattened pages.  The
+// lengths of sequences [sl_b0, sl_b0 + 32) come from a copy in shared memory.
 struct Walker {
   int b;
   long long sb, lo, hi;
   int w, G;
+  const int* sl;
+  int sl_b0;
   __device__ bool next(const DecodeArgs& a, Unit& u) {
     while (b < a.B && sb < hi) {
-      const int n = a.seq_lens[b];
+      const int n = (unsigned)(b - sl_b0) < 32u ? sl[b - sl_b0] : a.seq_lens[b];
       const int np = seq_pages(n, a.maxp, nullptr);
       const int bb = b;
       const long long s0 = sb;
@@ -128,6 +140,28 @@ struct Walker {
       }
     }
     return false;
+  }
+};
+
+// Addresses of the page ids of one worker range, in order.
+struct IdCursor {
+  Walker wk;
+  Unit u;
+  bool have;
+  int j;
+  __device__ IdCursor(const DecodeArgs& a, const Walker& w0) : wk(w0) {
+    have = wk.next(a, u);
+    j = have ? u.pb : 0;
+  }
+  // address of the next id; null past the end of the range
+  __device__ const int32_t* next(const DecodeArgs& a) {
+    if (!have) return nullptr;
+    const int32_t* p = a.page_table + (size_t)u.b * a.maxp + j;
+    if (++j >= u.pe) {
+      have = wk.next(a, u);
+      j = have ? u.pb : 0;
+    }
+    return p;
   }
 };
 
@@ -207,12 +241,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   __shared__ uint16_t mx_swap[2][2][128];  // row maxima between the two softmax warpgroups
   __shared__ uint32_t lsum_swap[2 * 128];  // row sums between them at the end of a unit
   __shared__ int page_ids[kIdRing];        // producer-private
+  __shared__ int sl_cache[32];             // lengths of the range's first sequences
+  __shared__ int touch_ids[kTouch];        // pages touched at start-up (producer)
 
   // launched as a dependent of the previous kernel on the stream: nothing is
   // read before that kernel has finished; the combine may launch right away
   grid_dep_wait();
   grid_dep_trigger();
   const uint32_t rank = cluster_rank(), peer = rank ^ 1u;
+
   const int w = blockIdx.x >> 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -247,6 +284,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(bar(B_MX), 256);
     mbar_init(bar(B_XSTAGED), 128);
     mbar_init(bar(B_XSTAGED + 1), 128);
+    mbar_init(bar(B_TOUCH), 1);
     mbar_expect_tx(bar(B_XFULL), kXBytes);
     mbar_expect_tx(bar(B_XFULL + 1), kXBytes);
     fence_mbar_init();
@@ -265,10 +303,52 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     int b0 = a.B;
     long long s0 = 0;
     if (lo < hi) warp_find_seq(a.seq_lens, a.B, a.maxp, lo, &b0, &s0);
+    // the lengths every role's walker reads first: kept in shared memory, so
+    // that no role waits on a global load behind the query loads at start-up
+    sl_cache[lane] = b0 + lane < a.B ? a.seq_lens[b0 + lane] : 0;
+    __syncwarp();
     if (lane == 0) {
       sh_P = P;
       sh_b0 = b0;
       sh_s0 = s0;
+      if (b0 < a.B) {  // the first sequence's query rows into L2 while the ids load
+        const uint32_t qb = (uint32_t)a.H * kLatent * 2;
+        const char* ql = reinterpret_cast<const char*>(a.q_lat + (size_t)b0 * a.H * kLatent);
+        for (uint32_t off = 0; off < qb; off += 16384) prefetch_l2(ql + off, min(16384u, qb - off));
+        prefetch_l2(a.q_pe + (size_t)b0 * a.H * kRope, (uint32_t)a.H * kRope * 2);
+      }
+      // the range's first kIdRing page ids, loaded together, so that the
+      // producer can start on its first page as soon as the CTA is set up
+      IdCursor ic(a, Walker{b0, s0, lo, hi, w, a.G, sl_cache, b0});
+      const int32_t* ptr[kIdRing];
+#pragma unroll
+      for (int i = 0; i < kIdRing; ++i) ptr[i] = ic.next(a);
+      // and the ids of the pages at range positions 31, 63, ... and of its
+      // last page, which the producer touches at start-up (see there)
+      const int32_t* tptr[kTouch] = {nullptr, nullptr, nullptr, nullptr};
+      if (lo < hi) {
+        Walker tw{b0, s0, lo, hi, w, a.G, sl_cache, b0};
+        Unit tu;
+        long long pos = lo, target = min(lo + 31, hi - 1);
+        int k = 0;
+        while (k < kTouch && target >= 0 && tw.next(a, tu)) {
+          const long long ue = pos + (tu.pe - tu.pb);
+          while (k < kTouch && target >= 0 && target < ue) {
+            tptr[k++] = a.page_table + (size_t)tu.b * a.maxp + tu.pb + (int)(target - pos);
+            target = target == hi - 1 ? -1 : min(target + 32, hi - 1);
+          }
+          pos = ue;
+        }
+      }
+      int v[kIdRing], tv[kTouch];
+#pragma unroll
+      for (int i = 0; i < kIdRing; ++i) v[i] = ptr[i] ? __ldg(ptr[i]) : -1;
+#pragma unroll
+      for (int i = 0; i < kTouch; ++i) tv[i] = tptr[i] ? __ldg(tptr[i]) : -1;
+#pragma unroll
+      for (int i = 0; i < kIdRing; ++i) page_ids[i] = v[i];
+#pragma unroll
+      for (int i = 0; i < kTouch; ++i) touch_ids[i] = tv[i];
     }
   }
   tc_fence_before();
@@ -277,7 +357,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
   const long long P = sh_P;
-  const Walker walker0{sh_b0, sh_s0, range_lo(w, a.G, P), range_lo(w + 1, a.G, P), w, a.G};
+  const Walker walker0{sh_b0, sh_s0, range_lo(w, a.G, P), range_lo(w + 1, a.G, P), w, a.G, sl_cache, sh_b0};
 
   // every lane waits, then the warp agrees, so warp-collective operations never
   // run with some lanes gone after an aborted wait
@@ -295,42 +375,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       Unit u;
       uint32_t g = 0;
       bool ok = true;
-      const uint32_t tx = rank == 0 ? 4 * kBox : 5 * kBox;
+      const uint32_t tx = 4 * kBox + kKpeBox;
       const long long lo = range_lo(w, a.G, P), hi = range_lo(w + 1, a.G, P);
       const uint32_t npages = hi > lo ? (uint32_t)(hi - lo) : 0u;
       // Page ids are read kIdRing positions ahead of the ring: the id of the
-      // worker's k-th page is kept in page_ids[k % kIdRing].  The first
-      // kIdRing ids are loaded together; afterwards one load per page is
+      // worker's k-th page is kept in page_ids[k % kIdRing].  Warp 3 loaded
+      // the first kIdRing ids in the prologue; afterwards one load per page is
       // issued and stored one page later, so no load latency sits in the loop.
-      Walker idw = walker0;
-      Unit iu;
-      bool id_have = idw.next(a, iu);
-      int ij = id_have ? iu.pb : 0;
-      auto id_next = [&]() -> const int32_t* {  // address of the next id, null past the end
-        if (!id_have) return nullptr;
-        const int32_t* p = a.page_table + (size_t)iu.b * a.maxp + ij;
-        if (++ij >= iu.pe) {
-          id_have = idw.next(a, iu);
-          ij = id_have ? iu.pb : 0;
-        }
-        return p;
-      };
-      {
-        const int32_t* ptr[kIdRing];
-#pragma unroll
-        for (int i = 0; i < kIdRing; ++i) ptr[i] = id_next();
-        int v[kIdRing];
-#pragma unroll
-        for (int i = 0; i < kIdRing; ++i) v[i] = ptr[i] ? __ldg(ptr[i]) : -1;
-#pragma unroll
-        for (int i = 0; i < kIdRing; ++i) page_ids[i] = v[i];
-      }
+      IdCursor ic(a, walker0);
+      for (int i = 0; i < kIdRing; ++i) ic.next(a);
       uint32_t id_count = kIdRing;  // ids loaded so far (one more may be in flight)
       int id_pend = -1;
       bool id_pend_ok = false;
       auto id_fetch = [&]() {
         if (id_pend_ok) page_ids[(id_count - 1) % kIdRing] = id_pend;  // loaded one page ago
-        const int32_t* p = id_next();
+        const int32_t* p = ic.next(a);
         id_pend_ok = true;
         id_pend = p ? __ldg(p) : -1;
         ++id_count;
@@ -342,10 +401,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // bf16: pages go straight into the stage ring.  E4M3: pages go into the
       // raw ring (codes and scales) and the exchange warps expand them.
       constexpr int kRing = kFp8 ? L::kRaw : kStages;
+      // Start-up touches (bf16): the first bulk copy that reads a 2 MB memory
+      // page no copy of this SM has read yet was measured to land about 10 us
+      // late once the stream is running (about 2 us at start-up), stalling the
+      // ring.  So at start-up one box of a page in each later memory page of
+      // the range is loaded into the last stage, whose first real load waits
+      // for them.  (L2 prefetches and ordinary loads did not help.)
+      bool touch_wait = false;
+      if (!kFp8 && npages >= (uint32_t)kStages) {
+        const uint32_t tst = base + (kStages - 1) * kStageBytes;
+        int nt = 0;
+        for (int i = 0; i < kTouch; ++i) nt += touch_ids[i] >= 0 && touch_ids[i] < a.num_pages;
+        if (nt > 0) {
+          mbar_expect_tx(bar(B_TOUCH), (uint32_t)nt * kBox);
+          for (int i = 0, k = 0; i < kTouch; ++i)
+            if (touch_ids[i] >= 0 && touch_ids[i] < a.num_pages)
+              tma_load_2d(tst + (k++) * kBox, &tm_ckv, bar(B_TOUCH), (int)rank * 256, touch_ids[i] * kPage);
+          touch_wait = true;
+        }
+      }
       while (ok && wk.next(a, u)) {
         for (int j = u.pb; j < u.pe; ++j, ++g) {
           const uint32_t s = g % kRing;
           const int free_bar = kFp8 ? B_RFREE : B_EMPTY, full_bar = kFp8 ? B_RFULL : B_FULL;
+          if (touch_wait && g == (uint32_t)kStages - 1) {
+            touch_wait = false;
+            if (!mbar_wait(bar(B_TOUCH), 0, &abort_flag, a.err)) {
+              ok = false;
+              break;
+            }
+          }
           if (g >= (uint32_t)kRing &&
               !mbar_wait(bar(free_bar + s), ((g / kRing) - 1) & 1, &abort_flag, a.err)) {
             ok = false;
@@ -356,10 +441,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint32_t fb = bar(full_bar + s);
           if (kFp8) {
             const uint32_t raw = base + L::kOffRaw + s * kRawBytes;
-            mbar_expect_tx(fb, 2 * 8192 + (rank == 1 ? 4096 : 0) + kPage * 4);
+            mbar_expect_tx(fb, 2 * 8192 + 2048 + kPage * 4);
             tma_load_2d(raw, &tm_ckv, fb, (int)rank * 256, page * kPage);
             tma_load_2d(raw + 8192, &tm_ckv, fb, (int)rank * 256 + 128, page * kPage);
-            if (rank == 1) tma_load_2d(raw + kRawKpe, &tm_kpe, fb, 0, page * kPage);
+            tma_load_2d(raw + kRawKpe, &tm_kpe, fb, (int)rank * 32, page * kPage);
             bulk_copy_g2s(raw + kRawScale, a.kv_scale + (size_t)page * kPage, kPage * 4, fb);
           } else {
             const uint32_t st = base + s * kStageBytes;
@@ -367,7 +452,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 4; ++i)
               tma_load_2d(st + i * kBox, &tm_ckv, fb, (int)rank * 256 + i * 64, page * kPage);
-            if (rank == 1) tma_load_2d(st + 4 * kBox, &tm_kpe, fb, 0, page * kPage);
+            tma_load_2d(st + 4 * kBox, &tm_kpe, fb, (int)rank * 32, page * kPage);
           }
           // keep the page ids kIdRing ahead.  (An L2 prefetch of the pages ahead
           // of the ring was measured to slow the stream down: the TMA loads
@@ -376,6 +461,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
       // copies still in flight must land before the CTA can exit
+      if (touch_wait) {
+        volatile int no_abort = 0;
+        mbar_wait(bar(B_TOUCH), 0, &no_abort, nullptr);
+      }
       for (uint32_t k = g > (uint32_t)kRing ? g - kRing : 0; k < g; ++k) {
         volatile int no_abort = 0;
         mbar_wait(bar((kFp8 ? B_RFULL : B_FULL) + k % kRing), (k / kRing) & 1, &no_abort, nullptr);
@@ -410,11 +499,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < 16; ++kk)
             mma_bf16_ts(d, tmem + kTmQ + kk * 8, kdesc + (uint64_t)(((kk >> 2) * kBox + (kk & 3) * 32) >> 4),
                         idesc_qk, kk > 0 ? 1u : 0u);
-          if (rank == 1) {
-            const uint64_t qdesc = sdesc_sw128(base + kOffQpe, 16, 1024);
-            const uint64_t rdesc = sdesc_sw128(st + 4 * kBox, 16, 1024);
+          {  // this CTA's 32 dimensions of the RoPE key: A = q_pe half (shared memory)
+            const uint64_t qdesc = sdesc_sw64(base + kOffQpe, 16, 512);
+            const uint64_t rdesc = sdesc_sw64(st + 4 * kBox, 16, 512);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) mma_bf16_ss(d, qdesc + kk * 2, rdesc + kk * 2, idesc_qk, 1u);
+            for (int kk = 0; kk < 2; ++kk) mma_bf16_ss(d, qdesc + kk * 2, rdesc + kk * 2, idesc_qk, 1u);
           }
           mma_commit(bar(B_SFULL));
           if (i == np - 1) mma_commit(bar(B_QFREE));
@@ -494,9 +583,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp < 8) {
     // ------------------------------------------------------------ exchange warps
     // Stage each page's partial score (log2 domain, fp16) in shared memory as
-    // soon as its S = Q K^T completes; one thread then hands the 16 KB to the
-    // async copy engine, which writes it into the peer CTA and completes the
-    // peer's receive barrier.  (Per-thread remote stores would queue behind
+    // soon as its S = Q K^T completes; one thread per warp then hands the
+    // warp's 4 KB to the async copy engine, which writes it into the peer CTA
+    // and completes the peer's receive barrier.  (Per-thread remote stores would queue behind
     // the SM-to-SM network and hold up the softmax warps' shared-memory
     // traffic.)
     const int h = threadIdx.x - 128;
@@ -527,17 +616,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         st_shared_v4(rowa + (((cb + 1) ^ (row & 7)) << 4), e4m3x2_to_bf16x2(v.z), e4m3x2_to_bf16x2(v.z >> 16),
                      e4m3x2_to_bf16x2(v.w), e4m3x2_to_bf16x2(v.w >> 16));
       }
-      if (rank == 1) {  // rope codes: 64 rows x 4 chunks
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const int q = h + 128 * i, row = q >> 2, cc = q & 3;
-          const uint4 v = ld_shared_v4u(raw + kRawKpe + row * 64 + cc * 16);
-          const uint32_t rowa = st + 4 * kBox + row * 128;
-          st_shared_v4(rowa + (((2 * cc) ^ (row & 7)) << 4), e4m3x2_to_bf16x2(v.x),
-                       e4m3x2_to_bf16x2(v.x >> 16), e4m3x2_to_bf16x2(v.y), e4m3x2_to_bf16x2(v.y >> 16));
-          st_shared_v4(rowa + (((2 * cc + 1) ^ (row & 7)) << 4), e4m3x2_to_bf16x2(v.z),
-                       e4m3x2_to_bf16x2(v.z >> 16), e4m3x2_to_bf16x2(v.w), e4m3x2_to_bf16x2(v.w >> 16));
-        }
+      {  // this CTA's 32 rope codes per token: 64 rows x 2 chunks of 16, into the
+         // 64-byte-swizzled k_pe box (16-byte chunk c of row r at c ^ ((r >> 1) & 3))
+        const int row = h >> 1, cc = h & 1, sw = (row >> 1) & 3;
+        const uint4 v = ld_shared_v4u(raw + kRawKpe + row * 32 + cc * 16);
+        const uint32_t rowa = st + 4 * kBox + row * 64;
+        st_shared_v4(rowa + (((2 * cc) ^ sw) << 4), e4m3x2_to_bf16x2(v.x), e4m3x2_to_bf16x2(v.x >> 16),
+                     e4m3x2_to_bf16x2(v.y), e4m3x2_to_bf16x2(v.y >> 16));
+        st_shared_v4(rowa + (((2 * cc + 1) ^ sw) << 4), e4m3x2_to_bf16x2(v.z), e4m3x2_to_bf16x2(v.z >> 16),
+                     e4m3x2_to_bf16x2(v.w), e4m3x2_to_bf16x2(v.w >> 16));
       }
       if (h < kPage / 4) {
         const uint4 v = ld_shared_v4u(raw + kRawScale + h * 16);
@@ -583,12 +670,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int cc = 0; cc < 8; ++cc)
           st_shared_v4(stg + x_off(h, cc), hx[4 * cc], hx[4 * cc + 1], hx[4 * cc + 2], hx[4 * cc + 3]);
         fence_proxy_async_smem();
-        mbar_arrive(bar(B_XSTAGED + sb));
-        if (h == 0) {
-          if (!mbar_wait(bar(B_XSTAGED + sb), (g >> 1) & 1, &abort_flag, a.err)) { ok = false; }
-          else bulk_copy_to_peer(x_peer + sb * kXBytes, stg, kXBytes, xfull_peer0 + sb * 8);
+        mbar_arrive(bar(B_XSTAGED + sb));  // for our own softmax warps
+        __syncwarp();
+        // each warp sends its own 32 rows (4 KB) as soon as they are staged;
+        // the peer's receive barrier completes when all four have landed
+        if (lane == 0) {
+          const uint32_t off = sb * kXBytes + (uint32_t)(warp & 3) * 4096u;
+          bulk_copy_to_peer(x_peer + off, base + kOffXs + off, 4096, xfull_peer0 + sb * 8);
         }
-        if (!__all_sync(0xffffffffu, ok)) break;
         // the next page's expansion waits for the P . V that frees its stage,
         // so it comes after this page's exchange
         if (kFp8 && g + 1 < npages && !expand(g + 1)) { ok = false; break; }
@@ -630,18 +719,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     auto load_q = [&](const Unit& q) {
       // this warpgroup's 128 latent values of the query half -> tensor memory
-      // columns [64j, 64j+64) (two bf16 per column); q_pe -> shared memory
+      // columns [64j, 64j+64) (two bf16 per column); this CTA's 32 values of
+      // q_pe -> shared memory (64-byte swizzle)
       // every load is issued before the first store, so the two global
       // round trips (latent and rope part) overlap
       const uint4* src = reinterpret_cast<const uint4*>(
           a.q_lat + ((size_t)q.b * H + h) * kLatent + rank * 256 + j * 128);
-      const uint4* sp = reinterpret_cast<const uint4*>(a.q_pe + ((size_t)q.b * H + h) * kRope);
-      const bool with_pe = rank == 1 && j == 0;
-      uint4 xq[16], xp[8];
+      const uint4* sp = reinterpret_cast<const uint4*>(a.q_pe + ((size_t)q.b * H + h) * kRope + rank * 32);
+      const bool with_pe = j == 0;
+      uint4 xq[16], xp[4];
 #pragma unroll
       for (int v = 0; v < 16; ++v) xq[v] = h < H ? src[v] : make_uint4(0, 0, 0, 0);
 #pragma unroll
-      for (int v = 0; v < 8; ++v) xp[v] = with_pe && h < H ? sp[v] : make_uint4(0, 0, 0, 0);
+      for (int v = 0; v < 4; ++v) xp[v] = with_pe && h < H ? sp[v] : make_uint4(0, 0, 0, 0);
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         uint32_t r[32];
@@ -656,8 +746,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       if (with_pe) {
 #pragma unroll
-        for (int cc = 0; cc < 8; ++cc)
-          st_shared_v4(base + kOffQpe + h * 128 + ((cc ^ (h & 7)) * 16), xp[cc].x, xp[cc].y, xp[cc].z, xp[cc].w);
+        for (int cc = 0; cc < 4; ++cc)
+          st_shared_v4(base + kOffQpe + h * 64 + ((cc ^ ((h >> 1) & 3)) * 16), xp[cc].x, xp[cc].y, xp[cc].z,
+                       xp[cc].w);
       }
       tmem_wait_st();
       fence_proxy_async_smem();
@@ -901,14 +992,15 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t stream) {
   const cuuint64_t cd[2] = {kLatent, rows}, cs[1] = {kLatent * es};
   const cuuint64_t kd[2] = {kRope, rows}, ks[1] = {kRope * es};
   if (fp8) {
-    const cuuint32_t cbox[2] = {128, 64}, kbox[2] = {64, 64};
+    const cuuint32_t cbox[2] = {128, 64}, kbox[2] = {32, 64};
     if (!make_tmap(&tc_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.ckv, cd, cs, cbox, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !make_tmap(&tk_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.kpe, kd, ks, kbox, CU_TENSOR_MAP_SWIZZLE_NONE))
       return cudaErrorInvalidValue;
   } else {
-    const cuuint32_t box[2] = {64, 64};
+    const cuuint32_t box[2] = {64, 64}, kbox[2] = {32, 64};
     if (!make_tmap(&tc_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.ckv, cd, cs, box) ||
-        !make_tmap(&tk_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.kpe, kd, ks, box))
+        !make_tmap(&tk_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.kpe, kd, ks, kbox,
+                   CU_TENSOR_MAP_SWIZZLE_64B))
       return cudaErrorInvalidValue;
   }
   auto kernel = fp8 ? decode_tc_kernel<true> : decode_tc_kernel<false>;

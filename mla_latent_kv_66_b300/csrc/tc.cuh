@@ -324,6 +324,12 @@ __device__ inline uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sb
   return d;
 }
 
+// Same with 64-byte swizzle (CU_TENSOR_MAP_SWIZZLE_64B: rows of 64 bytes,
+// 8-row / 512-byte atoms); K-major: lbo unused (16), sbo = 512.
+__device__ inline uint64_t sdesc_sw64(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (sdesc_sw128(saddr, lbo, sbo) & ~((uint64_t)7 << 61)) | ((uint64_t)4 << 61);
+}
+
 // Instruction descriptor, kind::f16 with bf16 A/B and fp32 D.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major) {
   return (1u << 4)                          // D format: f32
