@@ -52,9 +52,8 @@ def peaks():
 
 
 # DRAM bytes (read + write) of one decode launch, from one ncu capture of the
-# kernel as committed (profiles/decode_tc_v2_layer.md, decode_tc_fp8_batch.md);
-# None for workloads not captured.
-NCU_TRAFFIC_BYTES = {"v2_layer": 162.69e6, "fp8_batch": 655.14e6}
+# kernel as committed; None for workloads not captured.
+NCU_TRAFFIC_BYTES = {"v2_layer": 165.54e6, "fp8_batch": 656.02e6}
 
 
 def cache_bytes_per_token(kv_dtype):
