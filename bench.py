@@ -40,6 +40,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="v2_layer", choices=sorted(mi.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-seconds", type=float, default=60.0,
+                    help="host time of the reference arm's warm-up and timed steps together")
     return ap.parse_args()
 
 
@@ -151,6 +153,25 @@ def setup_gpu(w, device):
     return state, step
 
 
+def max_over_ranks(vals, world, device=None):
+    """Element-wise maximum over the ranks of per-rank timings: the slowest
+    replica sets the job's time.  One all-reduce; no-op for one process."""
+    vals = [float(v) for v in vals]
+    if world <= 1:
+        return vals
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(vals, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_tokens_per_s(world, tokens_per_step, ms):
+    """Whole-job throughput of `world` replicas that each decode
+    `tokens_per_step` tokens per step of `ms` milliseconds (the max over ranks)."""
+    return world * tokens_per_step / (ms / 1000.0)
+
+
 def run_ours(args, w, rank, world):
     import torch
     import torch.distributed as dist
@@ -213,10 +234,7 @@ def run_ours(args, w, rank, world):
         one((b_, c_))
     torch.cuda.synchronize()
     dms = statistics.mean(b_.elapsed_time(c_) for b_, c_ in dev_ev)
-    if world > 1:
-        t = torch.tensor([ms, dms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, dms = t.tolist()
+    ms, dms = max_over_ranks([ms, dms], world, dev)
 
     # end to end: pinned host inputs in, result out, through the public step call
     inp = st["inp"]
@@ -242,11 +260,7 @@ def run_ours(args, w, rank, world):
         d.synchronize()
         if i >= max(3, args.warmup):
             e2e_ms.append(a.elapsed_time(d))
-    e2e = statistics.mean(e2e_ms)
-    if world > 1:
-        t = torch.tensor([e2e], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e = t.item()
+    e2e, = max_over_ranks([statistics.mean(e2e_ms)], world, dev)
     status = step.status()
     return dict(ms=ms, dec_ms=dms, e2e_ms=e2e, h2d=h2d, d2h=d2h, wall=wall, clocks=clk.summary(),
                 status=status, G=G, tokens=int(inp["seq_lens"].sum()))
@@ -327,9 +341,9 @@ def cpu_oracle_sample(w, budget_s=15.0, seed=0):
 
 def run_reference(args, w):
     """The oracle as the reference arm: every step is a bounded sample of the
-    workload, sized so that warm-up plus timed steps take about a minute."""
+    workload, sized so that warm-up plus timed steps take about --ref-seconds."""
     s = OracleSample(w, 0)
-    per_step = min(20.0, max(0.02, 60.0 / (args.steps + max(3, args.warmup))))
+    per_step = min(20.0, max(0.02, args.ref_seconds / (args.steps + max(3, args.warmup))))
     for _ in range(max(3, args.warmup)):
         s.run(per_step)
     pairs, spent = 0, 0.0
@@ -375,7 +389,7 @@ def main():
         return
     hbm, tflops, src = peaks()
     tokens_per_step = w.B
-    value = world * tokens_per_step / (r["ms"] / 1000.0)
+    value = job_tokens_per_s(world, tokens_per_step, r["ms"])
     cache_bytes = r["tokens"] * cache_bytes_per_token(w.kv_dtype)
     achieved = cache_bytes / (r["dec_ms"] / 1000.0) / 1e9
     if w.kv_dtype == "bf16":
@@ -402,7 +416,7 @@ def main():
         "cached_tokens_per_s": r["tokens"] / (r["dec_ms"] / 1000.0),
         "roofline": roofline,
         "cpu_baseline": cpu,
-        "e2e": {"value": world * tokens_per_step / (r["e2e_ms"] / 1000.0), "unit": "tokens/s",
+        "e2e": {"value": job_tokens_per_s(world, tokens_per_step, r["e2e_ms"]), "unit": "tokens/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
         "gpu_launches": 4 * args.steps,
         "clocks": r["clocks"], "status": r["status"], "num_splits": r["G"], "wall_s_timed": r["wall"],
