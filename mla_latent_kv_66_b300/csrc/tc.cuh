@@ -45,15 +45,6 @@ __device__ inline void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
                : "memory");
 }
 
-// Arrive on the barrier at the same offset in CTA `rank` of this cluster.
-__device__ inline void mbar_arrive_cluster(uint32_t bar, uint32_t rank) {
-  asm volatile(
-      "{\n .reg .b32 ra;\n mapa.shared::cluster.u32 ra, %0, %1;\n"
-      " mbarrier.arrive.release.cluster.shared::cluster.b64 _, [ra];\n}\n" ::"r"(bar),
-      "r"(rank)
-      : "memory");
-}
-
 __device__ inline bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -124,19 +115,6 @@ __device__ inline void prefetch_l2(const void* p, uint32_t bytes) {
 
 __device__ inline void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
-}
-
-// 4-byte asynchronous copy global -> shared (no register dependency), one
-// commit group per call of cp_async_commit; cp_async_wait<N> returns once at
-// most N of this thread's most recent groups are still in flight.
-__device__ inline void cp_async_4(uint32_t dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src))
-               : "memory");
-}
-__device__ inline void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ inline void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // Make generic-proxy writes to shared memory visible to the async proxy
@@ -265,21 +243,7 @@ __device__ inline uint32_t mapa(uint32_t saddr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
   return r;
 }
-__device__ inline void st_cluster_v4(uint32_t caddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared::cluster.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(caddr), "r"(a), "r"(b), "r"(c),
-               "r"(d)
-               : "memory");
-}
-// Asynchronous 16-byte store into another CTA's shared memory; completes
-// 16 bytes of transaction count on that CTA's mbarrier (both addresses from
-// mapa).  No fence is needed: the receiver's wait on the mbarrier observes it.
-__device__ inline void st_async_v4(uint32_t caddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
-                                   uint32_t cbar) {
-  asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1,%2,%3,%4}, [%5];" ::"r"(caddr),
-      "r"(a), "r"(b), "r"(c), "r"(d), "r"(cbar)
-      : "memory");
-}
+
 // Bulk copy (by the async copy engine) of `bytes` from this CTA's shared
 // memory to another CTA's; both addresses 16-byte aligned, `bytes` a multiple
 // of 16.  Completes `bytes` of transaction count on the mbarrier `cbar` of
