@@ -131,6 +131,29 @@ def test_absorbed_equals_non_absorbed():
     assert np.allclose(lse_a, lse_b, rtol=0, atol=1e-10)
 
 
+def test_softmax_rows_sum_to_one_and_output_in_value_hull():
+    """Every probability row is a distribution (non-negative, sums to 1
+    within 1e-12; a single token gets probability 1), and the output is a
+    convex combination of the per-token values, so it lies between their
+    smallest and largest entries in every coordinate."""
+    inp = _tiny(B=3, H=4, lens=(1, 64, 700))
+    cache = O.build_cache(inp)
+    qpe = O.bf16_to_f64(O.rope_q_bf16(inp["q_pe_raw"], inp["seq_lens"]))
+    qn = O.bf16_to_f64(inp["q_nope"])
+    for b in range(3):
+        n = int(inp["seq_lens"][b])
+        c, kp = O.gather_sequence(cache, inp["page_table"], b, n)
+        for h in range(4):
+            wuv = O.bf16_to_f64(inp["w_uv"][h])
+            out, lse, p = O.decode_head(c, kp, qn[b, h], qpe[b, h], O.bf16_to_f64(inp["w_uk"][h]), wuv)
+            assert p.shape == (n,) and np.all(p >= 0)
+            assert abs(float(np.sum(p)) - 1.0) <= 1e-12
+            v = c @ wuv.T
+            assert np.all(out <= v.max(axis=0) + 1e-12) and np.all(out >= v.min(axis=0) - 1e-12)
+            if n == 1:
+                assert p[0] == 1.0
+
+
 def test_brute_force_triple_loop():
     rng = np.random.default_rng(3)
     n = 5
