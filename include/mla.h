@@ -86,9 +86,10 @@ int mla_version(void);
 /* ---------------------------------------------------------------------
  * mla_absorb_q: carry the no-position query into latent space.
  *   q_lat[b,h,:] = W_UK[h]^T q_nope[b,h,:]      (fp32 accumulate)
- * This is the key half of kv_b_proj (page: "kv_b_proj 把 512 维解压回 ...
- * Key 和 Value 分量") moved onto the query: q_nope.(W_UK,h c) =
- * (W_UK,h^T q_nope).c for every cached latent c.
+ * This is the key half of kv_b_proj (the up-projection of the 512-d latent
+ * into per-head keys and values; page section "源码里的压缩全流程")
+ * moved onto the query: q_nope.(W_UK,h c) = (W_UK,h^T q_nope).c for every
+ * cached latent c.
  *   q_nope : [B,H,128] bf16
  *   w_uk   : [H,128,512] bf16, (head, k_nope row, latent column)
  *   q_lat  : [B,H,512] bf16 output (round to nearest even)
@@ -131,8 +132,8 @@ void mla_workspace_offsets(const mla_params* p, int num_splits, size_t offsets[5
  *   s_t = softmax_scale * (q_lat[b,h].c_t + q_pe[b,h].k_pe_t)
  *   o_lat[b,h] = sum_t exp(s_t - lse) c_t,  lse[b,h] = log sum_t exp(s_t)
  * The 576-d score and the 512-d value sum read each cached byte once; all H
- * heads of a sequence share the cache tile (page: "k_pe 是全头共享的 ...
- * 避免了 128 份重复存储").  Every cached token is visible to the query
+ * heads of a sequence share the cache tile (the page's FAQ: one k_pe serves
+ * all 128 heads instead of 128 stored copies).  Every cached token is visible to the query
  * (decode of the newest token, whose own row is already in the cache).
  *   q_lat      : [B,H,512] bf16 (from mla_absorb_q)
  *   q_pe       : [B,H,64] bf16, already rotated at position n-1
@@ -173,9 +174,9 @@ mla_status mla_split_kv_combine(const mla_params* p, const void* workspace, size
 /* ---------------------------------------------------------------------
  * mla_out_proj: value up-projection after attention.
  *   out[b,h,:] = W_UV[h] o_lat[b,h,:]            (fp32 accumulate)
- * The value half of kv_b_proj (page: "512 维还原为每头 128 维的 k_nope 和
- * 128 维的 value"), applied once to the attention-weighted latent instead of
- * to every cached token.
+ * The value half of kv_b_proj (the latent restored to a 128-d key part and a
+ * 128-d value per head; page section "源码里的压缩全流程"), applied
+ * once to the attention-weighted latent instead of to every cached token.
  *   o_lat : [B,H,512] bf16;  w_uv : [H,128,512] bf16 (head, value row, latent)
  *   out   : [B,H,128] fp32 (MLA_OUT_F32) or bf16 (MLA_OUT_BF16)
  * Runs on the tensor cores (tcgen05, fp32 accumulation in tensor memory).
@@ -185,8 +186,9 @@ mla_status mla_out_proj(const mla_params* p, const void* o_lat, const void* w_uv
 
 /* ---------------------------------------------------------------------
  * mla_cache_append: write T new tokens into the paged cache (the step before
- * decode: "kv_a_proj_with_mqa ... 拆出 512 维潜变量和 64 维 k_pe",
- * "再经过 RMSNorm 归一化", RoPE on k_pe only, then "写入缓存").
+ * decode, page section "源码里的压缩全流程": the down-projection row is split into the
+ * 512-d latent and the 64-d k_pe, the latent is RMS-normalised, RoPE is
+ * applied to k_pe only, and both are written to the cache).
  *   kv_rows   : [T,576] bf16 down-projection rows (512 latent, 64 raw k_pe)
  *   slots     : [T] int32 physical slot, page*64 + offset
  *   positions : [T] int32 token positions for RoPE

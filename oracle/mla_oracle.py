@@ -29,7 +29,7 @@ import math
 import numpy as np
 
 D_LATENT, D_ROPE, D_NOPE, D_V, PAGE = 512, 64, 128, 128, 64
-D_QK = D_NOPE + D_ROPE  # 192: per-head query/key width [P3, "128 头 × 192 维"]
+D_QK = D_NOPE + D_ROPE  # 192: per-head query/key width [P3, model config: 128 heads of 192]
 ROPE_THETA = 10000.0
 
 
@@ -106,15 +106,16 @@ def f32_to_e4m3(x) -> np.ndarray:
 # cache write: RMSNorm on the latent, RoPE on the 64-d key part
 # --------------------------------------------------------------------------
 def rmsnorm(x) -> np.ndarray:
-    """RMSNorm of each row [P3: the 512-d latent "再经过 RMSNorm 归一化"].
+    """RMSNorm of each row [P3, section "MLA 的两个核心部件": the 512-d latent is
+    RMS-normalised before it is cached].
     Reading: gain 1 and eps 0 (the page gives neither): x / sqrt(mean(x^2))."""
     x = np.asarray(x, dtype=np.float64)
     return x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True))
 
 
 def rope(x, pos) -> np.ndarray:
-    """Rotary position embedding of the 64-d part [P3: "位置编码只作用在 64 维的
-    q_pe / k_pe 上"].  Reading (the pages do not fix the variant): half-split
+    """Rotary position embedding of the 64-d part [P3, section "MLA 的两个核心部件":
+    position encoding acts only on the 64-d q_pe / k_pe].  Reading (the pages do not fix the variant): half-split
     pairing, dimension i with i+32, angle pos * theta^(-i/32), theta = 10000,
     rotating each pair counter-clockwise:
         x'_i      = x_i cos(a) - x_{i+32} sin(a)

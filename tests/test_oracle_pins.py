@@ -292,10 +292,11 @@ def test_cache_accounting_against_page_table():
     assert acc["mla_total_bytes"] == 9_059_696_640
     assert acc["mha_total_bytes"] == 515_396_075_520
     assert math.isclose(acc["ratio"], 56.888, rel_tol=1e-4)
-    # the page's printed totals (1.87 TB, 1.75 GB, >1000x) are not reachable
-    # from its own counts: recorded, not asserted as truth
-    assert abs(acc["mla_total_bytes"] - 1.75e9) > 1e9
-    assert acc["ratio"] < 1000
+    # the page's printed totals (about 1.87 TB and 1.75 GB, over 1000x apart)
+    # are not reachable from its own counts: recorded, not asserted as truth
+    assert abs(acc["mla_total_bytes"] - g["printed_mla_total_bytes_approx"]) > 1e9
+    assert abs(acc["mha_total_bytes"] - g["printed_mha_total_bytes_approx"]) > 1e12
+    assert acc["ratio"] < g["printed_ratio_lower_bound"]
 
 
 # ---------------------------------------------------------------- generator
