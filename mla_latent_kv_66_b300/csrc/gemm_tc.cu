@@ -7,10 +7,9 @@
 // MLA page, section "源码里的压缩全流程", KV decompression) applied on the
 // query and output side.  Each CTA computes one head's [128 x N] tile, N =
 // the batch rounded up to 16, with the batch as the MMA's N dimension; the
-// weights stream once through a TMA
-// pipeline into 128-byte-swizzled shared memory, the accumulator lives in
-// tensor memory.  W_UK is read with its latent axis as M, i.e. as an
-// MN-major A operand; W_UV is K-major.
+// weights stream once through a TMA pipeline into 128-byte-swizzled shared
+// memory, the accumulator lives in tensor memory.  W_UK is read with its
+// latent axis as M, i.e. as an MN-major A operand; W_UV is K-major.
 #include "kernels.h"
 #include "tc.cuh"
 #include "tmap.cuh"
