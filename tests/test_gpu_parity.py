@@ -175,6 +175,35 @@ def test_split_counts_agree_within_tolerance():
     assert tol_ok(b, a, TOL_REL, TOL_ABS)[0]
 
 
+def test_combine_with_many_partials_per_sequence():
+    """More than 32 partials per sequence, some from empty worker ranges, in a
+    batch large enough for the grouped combine (one warp per head merging the
+    partials 32 at a time with a running maximum): sampled (sequence, head)
+    pairs against the oracle on exact q_lat, every output against the
+    unsplit run."""
+    lens = [4096 - 61 * b for b in range(19)]
+    inp = small_inputs(lens, H=128, seed=23)
+    cache = O.build_cache(inp)
+    qpe = O.rope_q_bf16(inp["q_pe_raw"], inp["seq_lens"])
+    qlat_bits = O.f64_to_bf16(O.absorb_q(inp["q_nope"], inp["w_uk"]))
+    pages = int(sum((n + 63) // 64 for n in lens))
+    r = run_gpu(inp, cache, qpe, 2 * pages, q_lat_bits=qlat_bits)  # every other worker range is empty
+    assert r["status"] == 0 and r["G"] == 2 * pages
+    whole = run_gpu(inp, cache, qpe, 1, q_lat_bits=qlat_bits)
+    assert whole["status"] == 0
+    got, ref_whole = to_f64(r["o_lat"]), to_f64(whole["o_lat"])
+    assert tol_ok(got.reshape(-1, 512), ref_whole.reshape(-1, 512), TOL_REL, TOL_ABS)[0]
+    assert np.allclose(to_f64(r["lse"]), to_f64(whole["lse"]), rtol=0, atol=1e-3)
+    qp, ql = O.bf16_to_f64(qpe), O.bf16_to_f64(qlat_bits)
+    for b in (0, 9, 18):
+        c, kp = O.gather_sequence(cache, inp["page_table"], b, lens[b])
+        for h in (0, 5, 64, 127):
+            o_ref, lse_ref = O.latent_attention(c, kp, ql[b, h], qp[b, h])
+            ok, err, bound = tol_ok(got[b, h], o_ref, TOL_REL, TOL_ABS)
+            assert ok, (b, h, err, bound)
+            assert abs(float(r["lse"][b, h]) - lse_ref) < 1e-3
+
+
 # ------------------------------------------------------------------ device-side error word
 def test_out_of_range_page_and_bad_length_set_the_error_word():
     inp = small_inputs([200, 100])
