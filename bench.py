@@ -53,9 +53,51 @@ def peaks():
     return 6400.0, 1800.0, "fallback"
 
 
-# DRAM bytes (read + write) of one decode launch, from one ncu capture of the
-# kernel as committed; None for workloads not captured.
-NCU_TRAFFIC_BYTES = {"v2_layer": 165.54e6, "fp8_batch": 656.02e6}
+# Sources of the decode kernel; their hash is recorded beside the ncu DRAM
+# traffic in profiles/, so a stale figure (kernel changed since the capture)
+# is reported as null.
+DECODE_SOURCES = ("mla_latent_kv_66_b300/csrc/decode_tc.cu", "mla_latent_kv_66_b300/csrc/tc.cuh",
+                  "mla_latent_kv_66_b300/csrc/common.cuh")
+CLOCK_WINDOW_S = 1.5  # the step repeated under the clock sampler before the timed steps
+
+
+def decode_source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for f in DECODE_SOURCES:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload):
+    """DRAM read + write bytes of one decode launch on this workload, from the
+    committed ncu summary (profiles/decode_tc_<workload>.md, lines
+    `traffic_bytes_per_launch: N` and `decode_source_hash: H`); None when
+    there is no capture or the kernel sources changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", f"decode_tc_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    for line in open(path):
+        line = line.strip().strip("`")
+        for key in ("traffic_bytes_per_launch", "decode_source_hash"):
+            if line.startswith(key + ":"):
+                vals[key] = line.split(":", 1)[1].strip()
+    if vals.get("decode_source_hash") != decode_source_hash() or "traffic_bytes_per_launch" not in vals:
+        return None
+    return float(vals["traffic_bytes_per_launch"])
+
+
+def host_cpu():
+    model = None
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except OSError:
+        pass
+    return os.cpu_count(), model
 
 
 def cache_bytes_per_token(kv_dtype):
@@ -208,7 +250,14 @@ def run_ours(args, w, rank, world):
     K = args.steps
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     with ClockSampler(dev.index) as clk:
-        torch.cuda.synchronize()
+        # the same step repeated for CLOCK_WINDOW_S under the sampler, so the
+        # clock record holds enough samples under this load even when K is small
+        t_end = time.perf_counter() + CLOCK_WINDOW_S
+        while time.perf_counter() < t_end:
+            for _ in range(50):
+                flush.zero_()
+                step.replay()
+            torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
         wall0 = time.perf_counter()
@@ -236,24 +285,37 @@ def run_ours(args, w, rank, world):
     dms = statistics.mean(b_.elapsed_time(c_) for b_, c_ in dev_ev)
     ms, dms = max_over_ranks([ms, dms], world, dev)
 
-    # end to end: pinned host inputs in, result out, through the public step call
+    # end to end: the step's per-token inputs (q_nope, rotated q_pe, page
+    # table, lengths) packed in one pinned host buffer, copied in with one
+    # host-to-device copy, the step, and the output copied back
     inp = st["inp"]
-    host = {k: st[k].cpu().pin_memory() for k in ("q_nope", "q_pe", "table", "lens")}
-    devb = {k: torch.empty_like(st[k]) for k in host}
+    names = ("q_nope", "q_pe", "table", "lens")
+    offs, total = {}, 0
+    for k in names:
+        offs[k] = total
+        total += (st[k].numel() * st[k].element_size() + 255) // 256 * 256
+    host_pack = torch.empty(total, dtype=torch.uint8).pin_memory()
+    dev_pack = torch.empty(total, dtype=torch.uint8, device=dev)
+
+    def view(buf, k):
+        n = st[k].numel() * st[k].element_size()
+        return buf[offs[k]: offs[k] + n].view(st[k].dtype).view(st[k].shape)
+
+    for k in names:
+        view(host_pack, k).copy_(st[k].cpu())
+    devb = {k: view(dev_pack, k) for k in names}
     out_h = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    h2d = sum(st[k].numel() * st[k].element_size() for k in names)
     d2h = out_h.numel() * out_h.element_size()
     e2e_ms = []
-    for k in host:  # the capture runs the step once: give it real inputs
-        devb[k].copy_(host[k])
+    dev_pack.copy_(host_pack)  # the capture runs the step once: give it real inputs
     step.capture(devb["q_nope"], devb["q_pe"], st["w_uk"], st["w_uv"], st["ckv"], st["kpe"], st["sc"],
                  devb["table"], devb["lens"])
     for i in range(max(3, args.warmup) + min(K, 500)):
         flush.zero_()
         a, d = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
-        for k in host:
-            devb[k].copy_(host[k], non_blocking=True)
+        dev_pack.copy_(host_pack, non_blocking=True)
         step.replay()
         out_h.copy_(step.out, non_blocking=True)
         d.record()
@@ -373,7 +435,7 @@ def main():
                           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                           "config": cfg,
                           "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                                           "sample": desc},
+                                           "sample": desc, "nproc": host_cpu()[0], "cpu_model": host_cpu()[1]},
                           "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                                   "d2h_bytes_per_step": 0}}), flush=True)
         return
@@ -401,12 +463,14 @@ def main():
         tf = flops / (r["dec_ms"] / 1000.0) / 1e12
         roofline = {"bound": "tensor", "achieved": tf, "peak": tflops, "unit": "TFLOP/s", "frac": tf / tflops,
                     "cache_gbs": achieved, "cache_frac_of_hbm": achieved / hbm}
-    roofline.update({"traffic": NCU_TRAFFIC_BYTES.get(w.name), "kernel": "mla_decode", "peak_source": src,
-                     "decode_ms": r["dec_ms"]})
+    roofline.update({"traffic": ncu_traffic(w.name), "kernel": "mla_decode", "peak_source": src,
+                     "decode_ms": r["dec_ms"], "decode_source_hash": decode_source_hash()})
     cpu = None
     if not args.no_cpu_baseline:
         v, cores, desc = cpu_oracle_sample(w)
-        cpu = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc}
+        nproc, model = host_cpu()
+        cpu = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc,
+               "nproc": nproc, "cpu_model": model}
     out = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": r["ms"], "higher_is_better": True, "scaling": "weak",

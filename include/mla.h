@@ -20,8 +20,9 @@
  * Conventions for every call:
  *  - All tensors are dense, row-major, contiguous, in device memory unless
  *    a comment says "host".  The caller owns every buffer and the stream.
- *  - No call allocates memory or synchronises, except mla_workspace_status,
- *    which reads one word back.  Calls only enqueue work on `stream`.
+ *  - No call allocates memory or synchronises, except mla_workspace_status
+ *    and mla_decode_static_status, which read one word back.  Calls only
+ *    enqueue work on `stream`.
  *  - Arguments are checked on the host; a bad argument returns
  *    MLA_ERR_INVALID_ARG (or MLA_ERR_UNSUPPORTED for a shape this build does
  *    not implement) and enqueues nothing.  A failed launch returns
@@ -230,18 +231,31 @@ mla_status mla_rope_q(const mla_params* p, const void* q_pe_raw, const int32_t* 
  *   partition count is the automatic one, lowered until the scratch fits.
  *   Returns MLA_ERR_WORKSPACE when even one partition does not fit (very
  *   large B*H); other host-side errors as mla_decode.
- *   Device-side input faults (bad page ids or lengths) are handled as in
- *   mla_decode but are not reported: the error word is in the shared array.
+ *   Device-side faults are handled as in mla_decode (a bad page id or
+ *   length skips that work; a bounded wait that runs out, an internal
+ *   fault, stops the kernel with MLA_ERR_TIMEOUT and leaves the outputs
+ *   partial).  They are recorded in the array's error word, which every
+ *   call clears when it starts: read it with mla_decode_static_status.
  * The first call on a device looks up the array's device address for that
- * device (once, with the device current); make that first call before any
- * stream capture.  All calls share the one array, and each call keeps the
- * previous call's contents until it overwrites them: calls that overlap on
- * the GPU (other streams, other threads) race and must be serialised by the
- * caller. */
+ * device (once, with the device current) and keeps it for the life of the
+ * process; make that first call before any stream capture.  A device reset
+ * (cudaDeviceReset) reloads the library's device image and invalidates the
+ * kept address: do not call this entry point after one.  All calls share
+ * the one array, and each call keeps the previous call's contents until it
+ * overwrites them: calls that overlap on the GPU (other streams, other
+ * threads) race and must be serialised by the caller. */
 mla_status mla_decode_static(const mla_params* p, const void* q_lat, const void* q_pe,
                              const void* ckv_cache, const void* kpe_cache, const float* kv_scale,
                              const int32_t* page_table, const int32_t* seq_lens, void* o_lat,
                              float* lse, mla_stream_t stream);
+
+/* mla_decode_static_status: the error word of mla_decode_static's fixed
+ * scratch, as a status (MLA_OK, MLA_ERR_PAGE_OOB, MLA_ERR_SEQ_LEN or
+ * MLA_ERR_TIMEOUT), for the most recent mla_decode_static call enqueued on
+ * `stream` (each call clears the word when it starts).  Copies the word to
+ * the host and synchronises `stream`; clears it when `clear` is non-zero.
+ * Allocates nothing. */
+mla_status mla_decode_static_status(int clear, mla_stream_t stream);
 
 /* mla_workspace_status: copy the workspace's sticky error word to the host
  * (synchronises `stream`) and return it as a status; clear it when `clear`

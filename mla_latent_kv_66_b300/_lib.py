@@ -62,6 +62,7 @@ _SIGS = {
     "mla_rope_q": (ctypes.c_int, [ctypes.POINTER(MlaParams), _P, _P, _P, _P]),
     "mla_workspace_status": (ctypes.c_int, [_P, ctypes.c_int, _P]),
     "mla_decode_static": (ctypes.c_int, [ctypes.POINTER(MlaParams), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "mla_decode_static_status": (ctypes.c_int, [ctypes.c_int, _P]),
 }
 
 
@@ -163,3 +164,8 @@ def mla_decode_static(p, q_lat, q_pe, ckv, kpe, kv_scale, page_table, seq_lens, 
     _check(lib.mla_decode_static(ctypes.byref(p), _ptr(q_lat), _ptr(q_pe), _ptr(ckv), _ptr(kpe), _ptr(kv_scale),
                                  _ptr(page_table), _ptr(seq_lens), _ptr(o_lat), _ptr(lse), _stream(stream)),
            "mla_decode_static")
+
+
+def mla_decode_static_status(clear=False, stream=None) -> int:
+    """Error word of mla_decode_static's fixed scratch (synchronises the stream)."""
+    return lib.mla_decode_static_status(1 if clear else 0, _stream(stream))

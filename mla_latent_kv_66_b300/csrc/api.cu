@@ -1,6 +1,7 @@
 // Host side of the libmla C ABI: argument checks, workspace layout, the
 // choice of KV partition count, and kernel launches.
 #include <math.h>
+#include <atomic>
 #include <string.h>
 
 #include "common.cuh"
@@ -11,23 +12,26 @@ using namespace mla;
 namespace {
 
 constexpr int kMaxDevices = 64;
-int g_workers[kMaxDevices];  // cached device property, 0 = not queried yet
+// cached device property, 0 = not queried yet.  Threads that race on the
+// first query compute the same value, so relaxed atomics suffice.
+std::atomic<int> g_workers[kMaxDevices];
 
 // Decode workers that run at once: co-resident clusters of the decode kernel
 // (one per pair of SMs where the GPCs allow it).
 int device_workers() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
-  if (g_workers[dev] == 0) {
-    int n = decode_tc_max_clusters();
+  int n = g_workers[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
+    n = decode_tc_max_clusters();
     if (n <= 0) {
       int sms = 0;
       if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
       n = sms / 2;
     }
-    g_workers[dev] = n;
+    g_workers[dev].store(n, std::memory_order_relaxed);
   }
-  return g_workers[dev];
+  return n;
 }
 
 mla_status check_params(const mla_params* p) {

@@ -6,6 +6,8 @@
 // splitting with its 128K contexts): for the partials s of one (sequence,
 // head), o = sum_s exp(lse_s - L) O_s with L = log sum_s exp(lse_s), each O_s
 // normalised over its own range.
+#include <atomic>
+
 #include "kernels.h"
 #include "tc.cuh"
 #include "tmap.cuh"
@@ -219,6 +221,22 @@ __global__ void __launch_bounds__(32 * kHeads) combine_group_kernel(const __nv_b
   if (lane == 0 && lse_out) lse_out[(size_t)b * H + h] = sum > 0.f ? m + logf(sum) : -INFINITY;
 }
 
+// SM count of the current device, cached per device (it only picks the
+// faster of two equivalent kernels, so a failed query falls back to 148).
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sms[kMaxDevices];
+
+int device_sm_count() {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return 148;
+  int n = g_sms[d].load(std::memory_order_relaxed);
+  if (n == 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d) != cudaSuccess || n <= 0) n = 148;
+    g_sms[d].store(n, std::memory_order_relaxed);
+  }
+  return n;
+}
+
 }  // namespace
 
 cudaError_t launch_combine(const __nv_bfloat16* part_o, const float* part_lse, const int* seq_start,
@@ -227,12 +245,7 @@ cudaError_t launch_combine(const __nv_bfloat16* part_o, const float* part_lse, c
   // than two of its CTAs per SM (few sequences, e.g. one long context whose
   // every worker holds a partial) the per-head form spreads the partials over
   // more SMs.
-  static int sms = [] {
-    int d = 0, n = 0;
-    if (cudaGetDevice(&d) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d) != cudaSuccess)
-      n = 148;
-    return n;
-  }();
+  const int sms = device_sm_count();
   const int groups = (H + kHeads - 1) / kHeads;
   if ((long long)B * groups >= 2LL * sms)
     return launch_dependent(combine_group_kernel, dim3(B, groups), dim3(32 * kHeads), 0, stream, part_o, part_lse,

@@ -63,3 +63,12 @@ extern "C" mla_status mla_decode_static(const mla_params* p, const void* q_lat, 
   if (s != MLA_OK) return s;
   return mla_split_kv_combine(p, ws, kStaticWsBytes, G, o_lat, lse, stream);
 }
+
+// The error word of the fixed scratch (offset 0, the same word mla_decode
+// keeps in a caller's workspace): read after a call of mla_decode_static on
+// the same stream.  Copies 4 bytes to the host and synchronises the stream.
+extern "C" mla_status mla_decode_static_status(int clear, mla_stream_t stream) {
+  void* ws = nullptr;
+  if (static_ws_address(&ws) != cudaSuccess) return MLA_ERR_CUDA;
+  return mla_workspace_status(ws, clear, stream);
+}

@@ -12,32 +12,35 @@
 //   rank 0: latent columns [0,256), k_pe [0,32);
 //   rank 1: latent columns [256,512), k_pe [32,64).
 // Each CTA TMA-loads only its part of every page (36 KB of the 72 KB) and
-// computes the partial score over its 288 of the 576 dimensions.  The two partial
-// score tiles are swapped through distributed shared memory in the log2
-// domain as fp16 (half the bytes of fp32; the SM-to-SM network, not HBM, is
-// the scarce resource here); each CTA adds its own staged fp16 partial to
-// the peer's, so both see the same scores and take the same softmax
-// decisions.  Each CTA then accumulates P . c over its own 256 latent
+// computes the partial score over its 288 of the 576 dimensions.  The two
+// fp32 partial score tiles (log2 domain) are swapped through distributed
+// shared memory by the async copy engine; each CTA adds its own partial to
+// the peer's, so both add the same two numbers exactly and take the same
+// softmax decisions.  Each CTA then accumulates P . c over its own 256 latent
 // columns.
 //
 // Warp roles (512 threads):
-//   warp 0       TMA producer (cache pages, 4-stage ring)
+//   warp 0       KV-partition schedule and the first page ids, then the TMA
+//                producer (cache pages, stage ring); its first loads are
+//                issued before the CTA-wide start-up barrier
 //   warp 1       MMA issuer for S = Q K^T (A = query in tensor memory)
-//   warp 2       tensor-memory allocation; then relays "exchange buffer
-//                consumed" to the peer CTA and re-arms the receive barrier
-//   warp 3       KV-partition schedule, the first page ids of the range,
-//                split records; then MMA issuer for
-//                O += P V (a separate issuer lets S = Q K^T run ahead)
+//   warp 2       tensor-memory allocation
+//   warp 3       split records; then MMA issuer for O += P V (a separate
+//                issuer lets S = Q K^T run ahead)
 //   warps 4..7   exchange: copy each partial score tile out of tensor memory
 //                as soon as its S = Q K^T completes (S has one buffer), stage
-//                it as fp16 in shared memory and send it to the peer CTA with
-//                one bulk copy per warp; double-buffered
+//                it in shared memory and send each warp's 32 rows to the peer
+//                CTA with one bulk copy (one tile each way, each row quarter
+//                on its own: warp q hands quarter q back to the peer as soon
+//                as its two softmax warps have read it); load each unit's
+//                query into tensor memory as soon as the previous unit's last
+//                S = Q K^T is done; E4M3 cache: expand the codes
 //   warps 8..15  two softmax warpgroups; warpgroup j owns tokens [32j, 32j+32)
-//                of every page, thread = head row: own staged fp16 partial +
-//                the peer's, row maximum agreed with the other warpgroup,
-//                online softmax with lazy rescaling, its half of P into tensor
-//                memory (two P buffers), its half of O rescaled when needed
-//                and written at the end of a unit.
+//                of every page, thread = head row: own staged partial + the
+//                peer's, row maximum agreed with the other warpgroup, online
+//                softmax with lazy rescaling, its half of P into tensor memory
+//                (two P buffers), its half of O rescaled when needed and
+//                written at the end of a unit.
 // Tensor memory: O [0,256), S [256,320), P double buffer [320,384) (bf16
 // pairs, the A operand of P . V), query [384,512).
 #include <cuda_fp16.h>
@@ -54,7 +57,10 @@ using namespace tc;
 constexpr uint32_t kBox = 8192;            // [64 rows x 64 bf16], 128-byte swizzle
 constexpr uint32_t kKpeBox = 4096;         // [64 rows x 32 bf16], 64-byte swizzle
 constexpr uint32_t kStageBf = 4 * kBox + kKpeBox;  // bf16 stage: 4 latent boxes + this CTA's k_pe half
-constexpr uint32_t kXBytes = 16384;        // [128 x 64] fp16 partial-score tile
+// Partial-score tile: [128 head rows x 64 tokens] fp32, as four slabs of 32
+// rows (one per exchange warp, 8 KB each).
+constexpr uint32_t kSlab = 32 * 256;
+constexpr uint32_t kXBytes = 4 * kSlab;
 // E4M3 cache: a raw page holds this CTA's 256 latent codes of 64 tokens as two
 // [64 x 128 B] boxes, its 32 rope codes ([64 x 32 B]) and the page's 64 fp32
 // scales; after expansion the bf16 stage also carries the scales.
@@ -64,45 +70,43 @@ constexpr int kMaxStages = 4;
 
 template <bool kFp8>
 struct Layout {
-  static constexpr int kStages = kFp8 ? 2 : 4;   // bf16 stages the MMAs read
+  static constexpr int kStages = kFp8 ? 3 : 4;   // bf16 stages the MMAs read
   static constexpr int kRaw = kFp8 ? 2 : 0;      // raw E4M3 pages
   static constexpr uint32_t kStageBytes = kFp8 ? kStageBf + 1024 : kStageBf;
   static constexpr uint32_t kOffRaw = kStages * kStageBytes;
   static constexpr uint32_t kOffQpe = kOffRaw + kRaw * kRawBytes;  // [128 x 32] bf16, 64-byte swizzle
-  static constexpr uint32_t kOffX = kOffQpe + 8192;                // 2 x peer partial scores
-  static constexpr uint32_t kOffXs = kOffX + 2 * kXBytes;          // 2 x own partial, outgoing
-  static constexpr uint32_t kSmemBytes = kOffXs + 2 * kXBytes + 1024;
+  static constexpr uint32_t kOffX = kOffQpe + 8192;                // the peer's partial score tile
+  static constexpr uint32_t kOffXs = kOffX + kXBytes;              // own partial, outgoing
+  static constexpr uint32_t kSmemBytes = kOffXs + kXBytes + 1024;
   static_assert(kStageBytes % 1024 == 0 && kRawBytes % 128 == 0 && kOffQpe % 512 == 0,
                 "swizzled tiles need 1024-byte (128 B swizzle) / 512-byte (64 B) alignment");
-  static_assert(kSmemBytes + 4096 <= 232448, "shared memory per CTA");
+  static_assert(kStages <= kMaxStages, "stage barriers");
+  static_assert(kSmemBytes + 4096 <= 232448, "shared memory per CTA (with the static part, < 4 KB)");
 };
 constexpr uint32_t kTmO = 0, kTmS = 256, kTmP = 320, kTmQ = 384;
 constexpr int kThreads = 512;
 constexpr float kRescaleLog2 = 8.f;  // lazy rescale threshold: P stays <= 2^8
 constexpr int kIdRing = 16;          // page ids read ahead by the producer
-constexpr int kTouch = 4;            // start-up touches: pages 32, 64, ... of the range and its last
 
 enum {
   B_FULL = 0,                       // bf16 stage ready (TMA landed, or E4M3 expanded)
   B_EMPTY = B_FULL + kMaxStages,    // bf16 stage consumed by P . V
   B_RFULL = B_EMPTY + kMaxStages,   // raw E4M3 page landed
   B_RFREE = B_RFULL + 2,            // raw E4M3 page expanded
-  B_SFULL = B_RFREE + 2,
-  B_SFREE = B_SFULL + 2,
-  B_XFULL = B_SFREE + 2,
-  B_XFREE = B_XFULL + 2,
-  B_XREAD = B_XFREE + 2,
-  B_PFULL = B_XREAD + 2,            // P buffer i written (tensor memory)
+  B_SFULL = B_RFREE + 2,            // S = Q K^T done
+  B_SFREE,                          // the exchange warps have read S
+  B_XSTG,                           // [4 row quarters] own slab staged (32 arrivals)
+  B_XFULL = B_XSTG + 4,             // [4] the peer's slab landed (local arm + its bulk copy)
+  B_XREAD = B_XFULL + 4,            // [4] the quarter's two softmax warps have read both slabs
+  B_XFREE = B_XREAD + 4,            // [4] the peer's softmax warps have read our slab
+  B_MX = B_XFREE + 4,               // [4] row-value swap between the quarter's two softmax warps
+  B_PFULL = B_MX + 4,               // [2] P buffer i written (tensor memory)
   B_PVD = B_PFULL + 2,              // the P . V that read P buffer i is done
   B_ODONE = B_PVD + 2,
   B_OFREE,
   B_QFULL,
-  B_QFREE,
   B_IDLE,
-  B_MX,
-  B_TOUCH,                          // start-up touches of the range's later memory pages landed
-  B_XSTAGED,
-  B_COUNT = B_XSTAGED + 2
+  B_COUNT
 };
 
 struct Unit {
@@ -143,27 +147,72 @@ struct Walker {
   }
 };
 
-// Addresses of the page ids of one worker range, in order.
-struct IdCursor {
+// The pages of one worker range, in order: (unit, page of the sequence).
+struct PageIter {
   Walker wk;
   Unit u;
   bool have;
   int j;
-  __device__ IdCursor(const DecodeArgs& a, const Walker& w0) : wk(w0) {
+  __device__ void start(const DecodeArgs& a, const Walker& w0) {
+    wk = w0;
     have = wk.next(a, u);
     j = have ? u.pb : 0;
   }
-  // address of the next id; null past the end of the range
-  __device__ const int32_t* next(const DecodeArgs& a) {
-    if (!have) return nullptr;
-    const int32_t* p = a.page_table + (size_t)u.b * a.maxp + j;
+  __device__ void advance(const DecodeArgs& a) {
     if (++j >= u.pe) {
       have = wk.next(a, u);
       j = have ? u.pb : 0;
     }
-    return p;
+  }
+  // address of the current page's id in the page table
+  __device__ const int32_t* id_ptr(const DecodeArgs& a) const {
+    return a.page_table + (size_t)u.b * a.maxp + j;
   }
 };
+
+// Run by one full warp, reading only the sequence lengths: the batch's total
+// page count P and, for worker w's first flattened page lo, the sequence b0
+// holding it and that sequence's first flattened page s0 (b0 = B for an empty
+// range).  Lane l stores the length of sequence b0 + l in sl[l] (0 past the
+// batch).  Invalid lengths count as 0 pages; they are reported later.
+__device__ inline void warp_schedule(const DecodeArgs& a, int w, long long* P_out, int* b0_out, long long* s0_out,
+                                     int* sl) {
+  const int lane = threadIdx.x & 31;
+  const int first = lane < a.B ? __ldg(a.seq_lens + lane) : 0;  // the first 32 lengths stay in registers
+  long long P = 0;
+  for (int base = 0; base < a.B; base += 32) {
+    const int n = base == 0 ? first : (base + lane < a.B ? __ldg(a.seq_lens + base + lane) : 0);
+    const int np = base + lane < a.B ? seq_pages(n, a.maxp, nullptr) : 0;
+    P += __shfl_sync(0xffffffffu, warp_incl_scan(np), 31);
+  }
+  const long long lo = range_lo(w, a.G, P), hi = range_lo(w + 1, a.G, P);
+  int b0 = a.B;
+  long long s0 = 0;
+  if (lo < hi) {
+    long long run = 0;
+    for (int base = 0; base < a.B; base += 32) {
+      const int b = base + lane;
+      const int n = base == 0 ? first : (b < a.B ? __ldg(a.seq_lens + b) : 0);
+      const int np = b < a.B ? seq_pages(n, a.maxp, nullptr) : 0;
+      const int incl = warp_incl_scan(np);
+      const long long st = run + incl - np;
+      const unsigned m = __ballot_sync(0xffffffffu, b < a.B && np > 0 && st <= lo && lo < st + np);
+      if (m) {
+        const int src = __ffs(m) - 1;
+        b0 = base + src;
+        s0 = __shfl_sync(0xffffffffu, st, src);
+        break;
+      }
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+  }
+  const int bl = b0 + lane;
+  const int from_regs = __shfl_sync(0xffffffffu, first, bl & 31);  // every lane takes part
+  sl[lane] = bl < a.B ? (bl < 32 ? from_regs : __ldg(a.seq_lens + bl)) : 0;
+  *P_out = P;
+  *b0_out = b0;
+  *s0_out = s0;
+}
 
 __device__ inline uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -191,14 +240,6 @@ __device__ inline uint32_t e4m3x2_to_bf16x2(uint32_t v) {
   const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
   return pack_bf16(f.x, f.y);
 }
-__device__ inline float4 ld_shared_v4f(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(addr)
-               : "memory");
-  return v;
-}
 __device__ inline float ld_shared_f32(uint32_t addr) {
   float v;
   asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
@@ -210,18 +251,48 @@ __device__ inline float ex2(float x) {
   return y;
 }
 
-// Byte offset of 16-byte chunk c (0..7) of score row h inside one exchange
-// buffer: a row is 64 fp16 values (128 bytes); the chunk order is rotated by
-// the row so that 8 consecutive rows touch 8 different bank groups.
-__device__ inline uint32_t x_off(int h, int c) { return (uint32_t)(h * 128 + ((c ^ (h & 7)) * 16)); }
-
-// Two fp32 values as one packed fp16 pair (round to nearest even), and back.
-__device__ inline uint32_t pack_h2(float lo, float hi) {
-  __half2 v = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
+// Byte offset of 16-byte chunk c (0..15, four fp32 scores) of score row h in
+// a partial-score tile.  Within each half-row the chunk order is rotated by
+// the row, so that 8 consecutive rows touch 8 different bank groups.
+__device__ inline uint32_t x_off(int h, int c) {
+  return (uint32_t)((h >> 5) * kSlab + (h & 31) * 256 + (((c & 8) | ((c & 7) ^ (h & 7))) * 16));
 }
-__device__ inline float2 unpack_h2(uint32_t u) {
-  return __half22float2(*reinterpret_cast<const __half2*>(&u));
+
+// Row h of this CTA's half of sequence b's query: latent columns
+// [128 hlo, 128 hhi) of the half (each 128 values fill 64 tensor-memory
+// columns, two bf16 per column) and, with_pe, the 32 RoPE values into shared
+// memory (64-byte swizzle, the A operand of the RoPE MMAs).  Rows h >= H are
+// zero.  The caller waits for the tensor-memory stores and publishes them.
+__device__ inline void load_q_rows(const DecodeArgs& a, uint32_t tq, uint32_t qpe, int b, int h, uint32_t rank,
+                                   int hlo, int hhi, bool with_pe) {
+  const bool on = h < a.H;
+  const uint4* src = reinterpret_cast<const uint4*>(a.q_lat + ((size_t)b * a.H + h) * kLatent + rank * 256);
+  const uint4* sp = reinterpret_cast<const uint4*>(a.q_pe + ((size_t)b * a.H + h) * kRope + rank * 32);
+  uint4 xp[4];
+#pragma unroll
+  for (int v = 0; v < 4; ++v) xp[v] = with_pe && on ? sp[v] : make_uint4(0, 0, 0, 0);
+  for (int half = hlo; half < hhi; ++half) {
+    uint4 xq[16];
+#pragma unroll
+    for (int v = 0; v < 16; ++v) xq[v] = on ? src[half * 16 + v] : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+      uint32_t r[32];
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        r[4 * v] = xq[cc * 8 + v].x;
+        r[4 * v + 1] = xq[cc * 8 + v].y;
+        r[4 * v + 2] = xq[cc * 8 + v].z;
+        r[4 * v + 3] = xq[cc * 8 + v].w;
+      }
+      tc::tmem_st32(tq + half * 64 + cc * 32, r);
+    }
+  }
+  if (with_pe) {
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc)
+      st_shared_v4(qpe + h * 64 + ((cc ^ ((h >> 1) & 3)) * 16), xp[cc].x, xp[cc].y, xp[cc].z, xp[cc].w);
+  }
 }
 
 template <bool kFp8>
@@ -232,27 +303,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   constexpr int kStages = L::kStages;
   constexpr uint32_t kStageBytes = L::kStageBytes;
   constexpr uint32_t kOffQpe = L::kOffQpe, kOffX = L::kOffX, kOffXs = L::kOffXs;
+  // bf16: pages go straight into the stage ring.  E4M3: pages go into the
+  // raw ring (codes and scales) and the exchange warps expand them.
+  constexpr int kRing = kFp8 ? L::kRaw : kStages;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bars[B_COUNT];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
   __shared__ long long sh_P, sh_s0;
   __shared__ int sh_b0;
-  __shared__ uint16_t mx_swap[2][2][128];  // row maxima between the two softmax warpgroups
+  __shared__ float mx_swap[2][2][128];     // row maxima between the two softmax warpgroups
   __shared__ uint32_t lsum_swap[2 * 128];  // row sums between them at the end of a unit
   __shared__ int page_ids[kIdRing];        // producer-private
   __shared__ int sl_cache[32];             // lengths of the range's first sequences
-  __shared__ int touch_ids[kTouch];        // pages touched at start-up (producer)
 
-  // launched as a dependent of the previous kernel on the stream: nothing is
-  // read before that kernel has finished; the combine may launch right away
-  grid_dep_wait();
-  grid_dep_trigger();
   const uint32_t rank = cluster_rank(), peer = rank ^ 1u;
-
   const int w = blockIdx.x >> 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  uint8_t* const smem_base = smem_raw + (base - smem_u32(smem_raw));  // the same aligned address, as a pointer
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   if (threadIdx.x == 0) {
@@ -267,10 +336,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar(B_SFULL), 1);
     mbar_init(bar(B_SFREE), 128);  // the exchange warps have read S
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(B_XFULL + i), 1);    // local arm + 16 KB of the peer's st.async
-      mbar_init(bar(B_XFREE + i), 1);    // the peer's relay: its buffer is consumed
-      mbar_init(bar(B_XREAD + i), 256);  // local softmax threads consumed buffer i
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(bar(B_XSTG + i), 32);   // the 32 lanes of one exchange warp
+      mbar_init(bar(B_XFULL + i), 1);   // local arm + one slab of the peer's bulk copy
+      mbar_init(bar(B_XREAD + i), 64);  // the quarter's two softmax warps
+      mbar_init(bar(B_XFREE + i), 1);   // the peer's exchange warp of this quarter
+      mbar_init(bar(B_MX + i), 64);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(B_PFULL + i), 256);
@@ -278,86 +349,110 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar(B_ODONE), 1);
     mbar_init(bar(B_OFREE), 256);
-    mbar_init(bar(B_QFULL), 256);
-    mbar_init(bar(B_QFREE), 1);
+    mbar_init(bar(B_QFULL), 256);  // the softmax threads (first unit) or the exchange threads twice
     mbar_init(bar(B_IDLE), 2);
-    mbar_init(bar(B_MX), 256);
-    mbar_init(bar(B_XSTAGED), 128);
-    mbar_init(bar(B_XSTAGED + 1), 128);
-    mbar_init(bar(B_TOUCH), 1);
-    mbar_expect_tx(bar(B_XFULL), kXBytes);
-    mbar_expect_tx(bar(B_XFULL + 1), kXBytes);
+    for (int i = 0; i < 4; ++i) mbar_expect_tx(bar(B_XFULL + i), kSlab);
     fence_mbar_init();
     prefetch_tmap(&tm_ckv);
     prefetch_tmap(&tm_kpe);
   }
-  if (warp == 2) {
-    tmem_alloc(smem_u32(&tmem_slot), 512);
-    tmem_relinquish();
-  }
-  if (warp == 3) {
-    const bool lead = w == 0 && rank == 0;
-    const long long P = warp_total_pages(a.seq_lens, a.B, a.maxp, lead ? a.err : nullptr,
-                                         lead ? a.seq_start : nullptr);
-    const long long lo = range_lo(w, a.G, P), hi = range_lo(w + 1, a.G, P);
-    int b0 = a.B;
-    long long s0 = 0;
-    if (lo < hi) warp_find_seq(a.seq_lens, a.B, a.maxp, lo, &b0, &s0);
-    // the lengths every role's walker reads first: kept in shared memory, so
-    // that no role waits on a global load behind the query loads at start-up
-    sl_cache[lane] = b0 + lane < a.B ? a.seq_lens[b0 + lane] : 0;
+
+  // ---------------------------------------------------------------- producer state
+  // Warp 0 works out the schedule and issues the first loads of the stage
+  // ring before the start-up barrier: they read only the lengths, the page
+  // table and the cache, none of which the preceding kernel on the stream
+  // (the query absorption) writes, so they may overlap it.
+  PageIter pit{};
+  uint32_t g_prod = 0, id_count = 0;
+  int id_pend = -1;
+  bool id_pend_ok = false;
+  PageIter ic{};  // id read-ahead cursor (kIdRing pages ahead of pit)
+  auto page_at = [&](uint32_t k) {
+    const int pg = page_ids[k % kIdRing];
+    return pg >= 0 && pg < a.num_pages ? pg : -1;
+  };
+  auto id_fetch = [&]() {  // stores the id loaded one page ago, loads the next one
+    if (id_pend_ok) page_ids[(id_count - 1) % kIdRing] = id_pend;
+    id_pend_ok = true;
+    id_pend = ic.have ? __ldg(ic.id_ptr(a)) : -1;
+    if (ic.have) ic.advance(a);
+    ++id_count;
+  };
+  auto issue = [&](uint32_t g) {
+    const uint32_t s = g % kRing;
+    int page = page_at(g);
+    if (page < 0) page = 0;  // a bad page id: masked by the softmax warps
+    if (kFp8) {
+      const uint32_t fb = bar(B_RFULL + s);
+      const uint32_t raw = base + L::kOffRaw + s * kRawBytes;
+      mbar_expect_tx(fb, 2 * 8192 + 2048 + kPage * 4);
+      tma_load_2d(raw, &tm_ckv, fb, (int)rank * 256, page * kPage);
+      tma_load_2d(raw + 8192, &tm_ckv, fb, (int)rank * 256 + 128, page * kPage);
+      tma_load_2d(raw + kRawKpe, &tm_kpe, fb, (int)rank * 32, page * kPage);
+      bulk_copy_g2s(raw + kRawScale, a.kv_scale + (size_t)page * kPage, kPage * 4, fb);
+    } else {
+      const uint32_t fb = bar(B_FULL + s);
+      const uint32_t st = base + s * kStageBytes;
+      mbar_expect_tx(fb, 4 * kBox + kKpeBox);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        tma_load_2d(st + i * kBox, &tm_ckv, fb, (int)rank * 256 + i * 64, page * kPage);
+      tma_load_2d(st + 4 * kBox, &tm_kpe, fb, (int)rank * 32, page * kPage);
+    }
+  };
+  if (warp == 0) {
+    long long P;
+    int b0;
+    long long s0;
+    warp_schedule(a, w, &P, &b0, &s0, sl_cache);
     __syncwarp();
     if (lane == 0) {
       sh_P = P;
       sh_b0 = b0;
       sh_s0 = s0;
-      if (b0 < a.B) {  // the first sequence's query rows into L2 while the ids load
-        const uint32_t qb = (uint32_t)a.H * kLatent * 2;
-        const char* ql = reinterpret_cast<const char*>(a.q_lat + (size_t)b0 * a.H * kLatent);
-        for (uint32_t off = 0; off < qb; off += 16384) prefetch_l2(ql + off, min(16384u, qb - off));
-        prefetch_l2(a.q_pe + (size_t)b0 * a.H * kRope, (uint32_t)a.H * kRope * 2);
-      }
-      // the range's first kIdRing page ids, loaded together, so that the
-      // producer can start on its first page as soon as the CTA is set up
-      IdCursor ic(a, Walker{b0, s0, lo, hi, w, a.G, sl_cache, b0});
+      const Walker w0{b0, s0, range_lo(w, a.G, P), range_lo(w + 1, a.G, P), w, a.G, sl_cache, b0};
+      pit.start(a, w0);
+      ic.start(a, w0);
+      // the range's first kIdRing page ids, loaded together
       const int32_t* ptr[kIdRing];
 #pragma unroll
-      for (int i = 0; i < kIdRing; ++i) ptr[i] = ic.next(a);
-      // and the ids of the pages at range positions 31, 63, ... and of its
-      // last page, which the producer touches at start-up (see there)
-      const int32_t* tptr[kTouch] = {nullptr, nullptr, nullptr, nullptr};
-      if (lo < hi) {
-        Walker tw{b0, s0, lo, hi, w, a.G, sl_cache, b0};
-        Unit tu;
-        long long pos = lo, target = min(lo + 31, hi - 1);
-        int k = 0;
-        while (k < kTouch && target >= 0 && tw.next(a, tu)) {
-          const long long ue = pos + (tu.pe - tu.pb);
-          while (k < kTouch && target >= 0 && target < ue) {
-            tptr[k++] = a.page_table + (size_t)tu.b * a.maxp + tu.pb + (int)(target - pos);
-            target = target == hi - 1 ? -1 : min(target + 32, hi - 1);
-          }
-          pos = ue;
-        }
+      for (int i = 0; i < kIdRing; ++i) {
+        ptr[i] = ic.have ? ic.id_ptr(a) : nullptr;
+        if (ic.have) ic.advance(a);
       }
-      int v[kIdRing], tv[kTouch];
+      int v[kIdRing];
 #pragma unroll
       for (int i = 0; i < kIdRing; ++i) v[i] = ptr[i] ? __ldg(ptr[i]) : -1;
 #pragma unroll
-      for (int i = 0; i < kTouch; ++i) tv[i] = tptr[i] ? __ldg(tptr[i]) : -1;
-#pragma unroll
       for (int i = 0; i < kIdRing; ++i) page_ids[i] = v[i];
-#pragma unroll
-      for (int i = 0; i < kTouch; ++i) touch_ids[i] = tv[i];
+      id_count = kIdRing;
+      // the ring's first pages need no free slot; their ids are all loaded,
+      // so the read-ahead of further ids starts after the start-up barrier
+      for (; pit.have && g_prod < (uint32_t)kRing; ++g_prod) {
+        issue(g_prod);
+        pit.advance(a);
+      }
     }
+  }
+  if (warp == 2) {
+    tmem_alloc(smem_u32(&tmem_slot), 512);
+    tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync();  // barrier inits visible to the peer before any remote arrive
+  // barrier inits visible to the peer before any remote arrive (a release
+  // arrive would also wait for the stage loads already in flight)
+  cluster_sync_relaxed();
   tc_fence_after();
+  // launched as a dependent of the previous kernel on the stream: the query
+  // and everything written below come after that kernel has finished
+  grid_dep_wait();
+  grid_dep_trigger();
   const uint32_t tmem = tmem_slot;
   const long long P = sh_P;
   const Walker walker0{sh_b0, sh_s0, range_lo(w, a.G, P), range_lo(w + 1, a.G, P), w, a.G, sl_cache, sh_b0};
+  const long long range_n = range_lo(w + 1, a.G, P) - range_lo(w, a.G, P);
+  const uint32_t npages = range_n > 0 ? (uint32_t)range_n : 0u;
 
   // every lane waits, then the warp agrees, so warp-collective operations never
   // run with some lanes gone after an aborted wait
@@ -371,103 +466,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      Walker wk = walker0;
-      Unit u;
-      uint32_t g = 0;
+      const int free_bar = kFp8 ? B_RFREE : B_EMPTY, full_bar = kFp8 ? B_RFULL : B_FULL;
       bool ok = true;
-      const uint32_t tx = 4 * kBox + kKpeBox;
-      const long long lo = range_lo(w, a.G, P), hi = range_lo(w + 1, a.G, P);
-      const uint32_t npages = hi > lo ? (uint32_t)(hi - lo) : 0u;
-      // Page ids are read kIdRing positions ahead of the ring: the id of the
-      // worker's k-th page is kept in page_ids[k % kIdRing].  Warp 3 loaded
-      // the first kIdRing ids in the prologue; afterwards one load per page is
-      // issued and stored one page later, so no load latency sits in the loop.
-      IdCursor ic(a, walker0);
-      for (int i = 0; i < kIdRing; ++i) ic.next(a);
-      uint32_t id_count = kIdRing;  // ids loaded so far (one more may be in flight)
-      int id_pend = -1;
-      bool id_pend_ok = false;
-      auto id_fetch = [&]() {
-        if (id_pend_ok) page_ids[(id_count - 1) % kIdRing] = id_pend;  // loaded one page ago
-        const int32_t* p = ic.next(a);
-        id_pend_ok = true;
-        id_pend = p ? __ldg(p) : -1;
-        ++id_count;
-      };
-      auto page_at = [&](uint32_t k) {
-        const int pg = page_ids[k % kIdRing];
-        return pg >= 0 && pg < a.num_pages ? pg : -1;
-      };
-      // bf16: pages go straight into the stage ring.  E4M3: pages go into the
-      // raw ring (codes and scales) and the exchange warps expand them.
-      constexpr int kRing = kFp8 ? L::kRaw : kStages;
-      // Start-up touches (bf16): the first bulk copy that reads a 2 MB memory
-      // page no copy of this SM has read yet was measured to land about 10 us
-      // late once the stream is running (about 2 us at start-up), stalling the
-      // ring.  So at start-up one box of a page in each later memory page of
-      // the range is loaded into the last stage, whose first real load waits
-      // for them.  (L2 prefetches and ordinary loads did not help.)
-      bool touch_wait = false;
-      if (!kFp8 && npages >= (uint32_t)kStages) {
-        const uint32_t tst = base + (kStages - 1) * kStageBytes;
-        int nt = 0;
-        for (int i = 0; i < kTouch; ++i) nt += touch_ids[i] >= 0 && touch_ids[i] < a.num_pages;
-        if (nt > 0) {
-          mbar_expect_tx(bar(B_TOUCH), (uint32_t)nt * kBox);
-          for (int i = 0, k = 0; i < kTouch; ++i)
-            if (touch_ids[i] >= 0 && touch_ids[i] < a.num_pages)
-              tma_load_2d(tst + (k++) * kBox, &tm_ckv, bar(B_TOUCH), (int)rank * 256, touch_ids[i] * kPage);
-          touch_wait = true;
+      for (; ok && pit.have; ++g_prod) {
+        const uint32_t s = g_prod % kRing;
+        if (g_prod >= (uint32_t)kRing &&
+            !mbar_wait(bar(free_bar + s), ((g_prod / kRing) - 1) & 1, &abort_flag, a.err)) {
+          ok = false;
+          break;
         }
-      }
-      while (ok && wk.next(a, u)) {
-        for (int j = u.pb; j < u.pe; ++j, ++g) {
-          const uint32_t s = g % kRing;
-          const int free_bar = kFp8 ? B_RFREE : B_EMPTY, full_bar = kFp8 ? B_RFULL : B_FULL;
-          if (touch_wait && g == (uint32_t)kStages - 1) {
-            touch_wait = false;
-            if (!mbar_wait(bar(B_TOUCH), 0, &abort_flag, a.err)) {
-              ok = false;
-              break;
-            }
-          }
-          if (g >= (uint32_t)kRing &&
-              !mbar_wait(bar(free_bar + s), ((g / kRing) - 1) & 1, &abort_flag, a.err)) {
-            ok = false;
-            break;
-          }
-          int page = page_at(g);
-          if (page < 0) page = 0;  // a bad page id: masked by the softmax warps
-          const uint32_t fb = bar(full_bar + s);
-          if (kFp8) {
-            const uint32_t raw = base + L::kOffRaw + s * kRawBytes;
-            mbar_expect_tx(fb, 2 * 8192 + 2048 + kPage * 4);
-            tma_load_2d(raw, &tm_ckv, fb, (int)rank * 256, page * kPage);
-            tma_load_2d(raw + 8192, &tm_ckv, fb, (int)rank * 256 + 128, page * kPage);
-            tma_load_2d(raw + kRawKpe, &tm_kpe, fb, (int)rank * 32, page * kPage);
-            bulk_copy_g2s(raw + kRawScale, a.kv_scale + (size_t)page * kPage, kPage * 4, fb);
-          } else {
-            const uint32_t st = base + s * kStageBytes;
-            mbar_expect_tx(fb, tx);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              tma_load_2d(st + i * kBox, &tm_ckv, fb, (int)rank * 256 + i * 64, page * kPage);
-            tma_load_2d(st + 4 * kBox, &tm_kpe, fb, (int)rank * 32, page * kPage);
-          }
-          // keep the page ids kIdRing ahead.  (An L2 prefetch of the pages ahead
-          // of the ring was measured to slow the stream down: the TMA loads
-          // alone keep enough bytes in flight.)
-          id_fetch();  // stores the id of page g + kIdRing - 1, loads the next one
-        }
+        issue(g_prod);
+        id_fetch();  // keeps the page ids ahead of the ring (kIdRing - kRing pages at least)
+        pit.advance(a);
       }
       // copies still in flight must land before the CTA can exit
-      if (touch_wait) {
+      for (uint32_t k = g_prod > (uint32_t)kRing ? g_prod - kRing : 0; k < g_prod; ++k) {
         volatile int no_abort = 0;
-        mbar_wait(bar(B_TOUCH), 0, &no_abort, nullptr);
-      }
-      for (uint32_t k = g > (uint32_t)kRing ? g - kRing : 0; k < g; ++k) {
-        volatile int no_abort = 0;
-        mbar_wait(bar((kFp8 ? B_RFULL : B_FULL) + k % kRing), (k / kRing) & 1, &no_abort, nullptr);
+        mbar_wait(bar(full_bar + k % kRing), (k / kRing) & 1, &no_abort, nullptr);
       }
     }
   } else if (warp == 1) {
@@ -505,8 +520,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < 2; ++kk) mma_bf16_ss(d, qdesc + kk * 2, rdesc + kk * 2, idesc_qk, 1u);
           }
+          // completes once every MMA issued so far is done, including all of this
+          // unit's reads of the query when i is its last page
           mma_commit(bar(B_SFULL));
-          if (i == np - 1) mma_commit(bar(B_QFREE));
         }
         g += np;
         ++uc;
@@ -516,23 +532,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_wait(bar(B_IDLE), 0, &no_abort, nullptr);
     }
   } else if (warp == 2) {
-    // ------------------------------------------------------------ exchange relay
-    if (lane == 0) {
-      const uint32_t xfree_peer0 = mapa(bar(B_XFREE), peer);
-      Walker wk = walker0;
-      Unit u;
-      uint32_t g = 0;
-      bool ok = true;
-      while (ok && wk.next(a, u)) {
-        for (int j = u.pb; j < u.pe; ++j, ++g) {
-          const uint32_t sb = g & 1;
-          if (!mbar_wait(bar(B_XREAD + sb), (g >> 1) & 1, &abort_flag, a.err)) { ok = false; break; }
-          mbar_expect_tx(bar(B_XFULL + sb), kXBytes);  // arm for page g+2
-          mbar_arrive_remote(xfree_peer0 + sb * 8);     // the peer may refill it
-        }
-      }
-    }
+    // tensor-memory allocation only (done at start-up)
   } else if (warp == 3) {
+    // the batch's page offsets and the length check (written once, by the
+    // first CTA), then the split records of this worker
+    if (w == 0 && rank == 0) warp_total_pages(a.seq_lens, a.B, a.maxp, a.err, a.seq_start);
     if (lane == 0) {
       // ---------------------------------------------------------- split records
       if (rank == 0) {
@@ -582,19 +586,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   } else if (warp < 8) {
     // ------------------------------------------------------------ exchange warps
-    // Stage each page's partial score (log2 domain, fp16) in shared memory as
-    // soon as its S = Q K^T completes; one thread per warp then hands the
-    // warp's 4 KB to the async copy engine, which writes it into the peer CTA
-    // and completes the peer's receive barrier.  (Per-thread remote stores would queue behind
-    // the SM-to-SM network and hold up the softmax warps' shared-memory
-    // traffic.)
+    // Copy each page's partial score (log2 domain, fp32) out of tensor
+    // memory as soon as its S = Q K^T completes, stage it in shared memory,
+    // and hand each warp's slab of 32 rows to the async copy engine, which
+    // writes it into the peer CTA and completes the peer's receive barrier
+    // for that slab.  (Per-thread remote loads or stores would queue behind
+    // the SM-to-SM network.)
+    const int q4 = warp & 3;
     const int h = threadIdx.x - 128;
-    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const int H = a.H;
+    const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
+    const uint32_t xfull_peer = mapa(bar(B_XFULL), peer);
+    const uint32_t xfree_peer = mapa(bar(B_XFREE), peer);
     const uint32_t x_peer = mapa(base + kOffX, peer);
-    const uint32_t xfull_peer0 = mapa(bar(B_XFULL), peer);
     const float c = a.scale_log2;
-    const long long lo = range_lo(w, a.G, P), hi = range_lo(w + 1, a.G, P);
-    const uint32_t npages = hi > lo ? (uint32_t)(hi - lo) : 0u;
+
+    // this CTA's half of a later unit's query: 256 latent values -> tensor
+    // memory, 32 RoPE values -> shared memory
+    auto load_q = [&](const Unit& q) {
+      load_q_rows(a, tmem + lane_base + kTmQ, base + kOffQpe, q.b, h, rank, 0, 2, true);
+      tmem_wait_st();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive_cnt(bar(B_QFULL), 2);
+    };
+    // a later unit's query rows into L2 while this unit runs
+    auto prefetch_q = [&](int b) {
+      if (h != 0) return;
+      const uint32_t qb = (uint32_t)H * kLatent * 2;
+      const char* ql = reinterpret_cast<const char*>(a.q_lat + (size_t)b * H * kLatent);
+      for (uint32_t off = 0; off < qb; off += 16384) prefetch_l2(ql + off, min(16384u, qb - off));
+      prefetch_l2(a.q_pe + (size_t)b * H * kRope, (uint32_t)H * kRope * 2);
+    };
 
     // E4M3 only: expand raw page gc into bf16 stage gc % kStages (exact
     // conversion, same 128-byte-swizzled layout TMA gives the bf16 cache) and
@@ -640,120 +663,106 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     Unit u;
     uint32_t g = 0;
     bool ok = true;
+    bool have = wk.next(a, u);
+    if (have) {  // the first unit's query is loaded by the softmax warps
+      Walker pk = wk;
+      Unit nu;
+      if (pk.next(a, nu)) prefetch_q(nu.b);
+    }
     if (kFp8 && npages > 0) ok = expand(0);
-    while (ok && wk.next(a, u)) {
+    while (ok && have) {
+      Walker pk = wk;  // the next unit, if any
+      Unit nu;
+      const bool have_next = pk.next(a, nu);
+      if (g > 0 && have_next) prefetch_q(nu.b);
       for (int jp = u.pb; jp < u.pe; ++jp, ++g) {
-        const uint32_t sb = g & 1;
         if (!wwait(B_SFULL, g & 1)) { ok = false; break; }
         tc_fence_after();
-        uint32_t hx[32];
+        float v[64];
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           uint32_t s32[32];
           tmem_ld32(tmem + lane_base + kTmS + half * 32, s32);
           tmem_wait_ld();
 #pragma unroll
-          for (int k = 0; k < 16; ++k)
-            hx[half * 16 + k] = pack_h2(__uint_as_float(s32[2 * k]) * c, __uint_as_float(s32[2 * k + 1]) * c);
+          for (int k = 0; k < 32; ++k) v[half * 32 + k] = __uint_as_float(s32[k]) * c;
         }
         tc_fence_before();
         mbar_arrive(bar(B_SFREE));
-        // staging buffer sb and the peer's buffer sb are free once the peer has
-        // consumed page g-2 (its copy has then finished reading ours) and our
-        // own softmax warps have read page g-2 from staging
-        if (g >= 2 && (!wwait_c(B_XFREE + sb, ((g >> 1) - 1) & 1) || !wwait(B_XREAD + sb, ((g >> 1) - 1) & 1))) {
-          ok = false;
-          break;
-        }
-        const uint32_t stg = base + kOffXs + sb * kXBytes;
+        if constexpr (kFp8) {
+          // E4M3: the score of token t is scale_t times the score of its codes
+          // (scales copied next to the expanded stage)
+          const float* sca = reinterpret_cast<const float*>(smem_base + (g % kStages) * kStageBytes + kStageScale);
 #pragma unroll
-        for (int cc = 0; cc < 8; ++cc)
-          st_shared_v4(stg + x_off(h, cc), hx[4 * cc], hx[4 * cc + 1], hx[4 * cc + 2], hx[4 * cc + 3]);
-        fence_proxy_async_smem();
-        mbar_arrive(bar(B_XSTAGED + sb));  // for our own softmax warps
-        __syncwarp();
-        // each warp sends its own 32 rows (4 KB) as soon as they are staged;
-        // the peer's receive barrier completes when all four have landed
-        if (lane == 0) {
-          const uint32_t off = sb * kXBytes + (uint32_t)(warp & 3) * 4096u;
-          bulk_copy_to_peer(x_peer + off, base + kOffXs + off, 4096, xfull_peer0 + sb * 8);
+          for (int k = 0; k < 64; ++k) v[k] *= sca[k];
         }
+        if (g >= 1) {
+          // our receive slab of this quarter is free once our softmax warps have
+          // read page g-1 from it: arm it for page g and tell the peer
+          if (!wwait(B_XREAD + q4, (g - 1) & 1)) { ok = false; break; }
+          if (lane == 0) {
+            mbar_expect_tx(bar(B_XFULL + q4), kSlab);
+            mbar_arrive_remote(xfree_peer + q4 * 8);
+          }
+          // our outgoing slab (and the peer's receive slab) is free once the
+          // peer's softmax warps have read page g-1
+          if (!wwait_c(B_XFREE + q4, (g - 1) & 1)) { ok = false; break; }
+        }
+        uint8_t* xt = smem_base + kOffXs;
+#pragma unroll
+        for (int cc = 0; cc < 16; ++cc)
+          *reinterpret_cast<float4*>(xt + x_off(h, cc)) = make_float4(v[4 * cc], v[4 * cc + 1], v[4 * cc + 2], v[4 * cc + 3]);
+        fence_proxy_async_smem();
+        mbar_arrive(bar(B_XSTG + q4));  // for our own softmax warps
+        __syncwarp();
+        // each warp sends its own slab as soon as it is staged
+        if (lane == 0) {
+          const uint32_t off = (uint32_t)q4 * kSlab;
+          bulk_copy_to_peer(x_peer + off, base + kOffXs + off, kSlab, xfull_peer + q4 * 8);
+        }
+        // the next unit's query goes in once this unit's last S = Q K^T is done
+        if (jp == u.pe - 1 && have_next) load_q(nu);
         // the next page's expansion waits for the P . V that frees its stage,
         // so it comes after this page's exchange
         if (kFp8 && g + 1 < npages && !expand(g + 1)) { ok = false; break; }
       }
+      if (!ok) break;
+      u = nu;
+      have = have_next;
+      wk = pk;
     }
   } else {
     // ------------------------------------------------------------ softmax warpgroups
     // Warpgroup j (warps 8+4j .. 11+4j) owns score columns [32j, 32j+32) of
     // every page (its 32 tokens) for all 128 head rows; thread = head row =
-    // tensor-memory lane.  It adds its own fp32 partial score to the peer's
-    // fp16 one and agrees on the row maximum with the other warpgroup.
+    // tensor-memory lane.  It adds its own CTA's partial score to the peer's
+    // and agrees on the row maximum with the other warpgroup.
     const int j = (warp - 8) >> 2;
-    const int h = (warp & 3) * 32 + lane;
-    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const int q4 = warp & 3;
+    const int h = q4 * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
     const int H = a.H;
     uint32_t xk = 0;  // phases of the warpgroup-exchange barrier consumed
 
-    // Swap one value per row with the other warpgroup (bounded wait).  Row
-    // maxima travel as fp16 bit patterns and alternate between two slots, so
-    // that a fast warpgroup cannot overwrite a value the other has not read
-    // yet.
-    auto swap_max = [&](uint32_t mine, uint32_t& other) -> bool {
+    // Swap one value per row with the other warpgroup's warp of the same row
+    // quarter (bounded wait).  Row maxima alternate between two slots, so that
+    // a fast warp cannot overwrite a value the other has not read yet.
+    auto swap_max = [&](float mine, float& other) -> bool {
       const uint32_t slot = xk & 1;
-      mx_swap[slot][j][h] = (uint16_t)mine;
-      mbar_arrive(bar(B_MX));
-      const bool okw = wwait(B_MX, xk & 1);
+      mx_swap[slot][j][h] = mine;
+      mbar_arrive(bar(B_MX + q4));
+      const bool okw = wwait(B_MX + q4, xk & 1);
       ++xk;
       other = mx_swap[slot][j ^ 1][h];
       return okw;
     };
     auto swap_sum = [&](uint32_t mine, uint32_t& other) -> bool {
       lsum_swap[j * 128 + h] = mine;
-      mbar_arrive(bar(B_MX));
-      const bool okw = wwait(B_MX, xk & 1);
+      mbar_arrive(bar(B_MX + q4));
+      const bool okw = wwait(B_MX + q4, xk & 1);
       ++xk;
       other = lsum_swap[(j ^ 1) * 128 + h];
       return okw;
-    };
-
-    auto load_q = [&](const Unit& q) {
-      // this warpgroup's 128 latent values of the query half -> tensor memory
-      // columns [64j, 64j+64) (two bf16 per column); this CTA's 32 values of
-      // q_pe -> shared memory (64-byte swizzle)
-      // every load is issued before the first store, so the two global
-      // round trips (latent and rope part) overlap
-      const uint4* src = reinterpret_cast<const uint4*>(
-          a.q_lat + ((size_t)q.b * H + h) * kLatent + rank * 256 + j * 128);
-      const uint4* sp = reinterpret_cast<const uint4*>(a.q_pe + ((size_t)q.b * H + h) * kRope + rank * 32);
-      const bool with_pe = j == 0;
-      uint4 xq[16], xp[4];
-#pragma unroll
-      for (int v = 0; v < 16; ++v) xq[v] = h < H ? src[v] : make_uint4(0, 0, 0, 0);
-#pragma unroll
-      for (int v = 0; v < 4; ++v) xp[v] = with_pe && h < H ? sp[v] : make_uint4(0, 0, 0, 0);
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        uint32_t r[32];
-#pragma unroll
-        for (int v = 0; v < 8; ++v) {
-          r[4 * v] = xq[cc * 8 + v].x;
-          r[4 * v + 1] = xq[cc * 8 + v].y;
-          r[4 * v + 2] = xq[cc * 8 + v].z;
-          r[4 * v + 3] = xq[cc * 8 + v].w;
-        }
-        tmem_st32(tmem + lane_base + kTmQ + j * 64 + cc * 32, r);
-      }
-      if (with_pe) {
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
-          st_shared_v4(base + kOffQpe + h * 64 + ((cc ^ ((h >> 1) & 3)) * 16), xp[cc].x, xp[cc].y, xp[cc].z,
-                       xp[cc].w);
-      }
-      tmem_wait_st();
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(bar(B_QFULL));
     };
 
     Walker wk = walker0;
@@ -761,14 +770,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint32_t g = 0, uc = 0;
     bool ok = true;
     bool have = wk.next(a, u);
-    if (have) load_q(u);
+    if (have) {  // the first unit's query: warpgroup j loads half j of the latent part
+      load_q_rows(a, tmem + lane_base + kTmQ, base + kOffQpe, u.b, h, rank, j, j + 1, j == 0);
+      tmem_wait_st();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(B_QFULL));
+    }
     while (ok && have) {
       const int np = u.pe - u.pb;
       float m = -INFINITY, l = 0.f;
       const int32_t* ptab = a.page_table + (size_t)u.b * a.maxp;
       int page_nx = ptab[u.pb];
       for (int i = 0; i < np; ++i) {
-        const uint32_t gi = g + i, sb = gi & 1, s = gi % kStages;
+        const uint32_t gi = g + i, s = gi % kStages;
         const int jp = u.pb + i;
         // page ids are read one page ahead: a global load's latency stays off
         // the softmax's critical path
@@ -778,40 +793,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int valid = page_ok ? min(kPage, u.n - jp * kPage) : 0;
         if (!page_ok && h == 0 && j == 0 && rank == 0) set_error(a.err, MLA_ERR_PAGE_OOB);
 
-        // score in the log2 domain: own partial (staged by the exchange warps)
-        // plus the peer's, both fp16; both CTAs add the same two numbers
-        if (!wwait_c(B_XFULL + sb, (gi >> 1) & 1) || !wwait(B_XSTAGED + sb, (gi >> 1) & 1)) {
+        // score in the log2 domain: own fp32 partial (staged by the exchange
+        // warps) plus the peer's; both CTAs add the same two numbers
+        if (!wwait(B_XSTG + q4, gi & 1) || !wwait_c(B_XFULL + q4, gi & 1)) {
           ok = false;
           break;
         }
         float x[32];
-        const uint32_t xbuf = base + kOffX + sb * kXBytes, obuf = base + kOffXs + sb * kXBytes;
+        {
+          const uint8_t* xb = smem_base + kOffX;
+          const uint8_t* ob = smem_base + kOffXs;
+          float4 pv[8], ov[8];
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          const uint4 v = ld_shared_v4u(xbuf + x_off(h, 4 * j + cc));
-          const uint4 o = ld_shared_v4u(obuf + x_off(h, 4 * j + cc));
-          const uint32_t pv[4] = {v.x, v.y, v.z, v.w}, ov[4] = {o.x, o.y, o.z, o.w};
+          for (int cc = 0; cc < 8; ++cc) {
+            pv[cc] = *reinterpret_cast<const float4*>(xb + x_off(h, 8 * j + cc));
+            ov[cc] = *reinterpret_cast<const float4*>(ob + x_off(h, 8 * j + cc));
+          }
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 b2 = unpack_h2(pv[e]), a2 = unpack_h2(ov[e]);
-            const int k = 8 * cc + 2 * e;
-            x[k] = a2.x + b2.x;
-            x[k + 1] = a2.y + b2.y;
+          for (int cc = 0; cc < 8; ++cc) {
+            x[4 * cc] = ov[cc].x + pv[cc].x;
+            x[4 * cc + 1] = ov[cc].y + pv[cc].y;
+            x[4 * cc + 2] = ov[cc].z + pv[cc].z;
+            x[4 * cc + 3] = ov[cc].w + pv[cc].w;
           }
         }
-        mbar_arrive(bar(B_XREAD + sb));  // relayed to the peer by warp 2
-        // E4M3: the score of token t is scale_t times the score of its codes
-        const uint32_t sca = base + s * kStageBytes + kStageScale + j * 128;
+        mbar_arrive(bar(B_XREAD + q4));  // the exchange warp of this quarter tells the peer
+        const uint32_t sca = base + s * kStageBytes + kStageScale + j * 128;  // E4M3 token scales
         if constexpr (kFp8) {
           if (!wwait(B_FULL + s, (gi / kStages) & 1)) { ok = false; break; }  // scales visible
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const float4 v = ld_shared_v4f(sca + q * 16);
-            x[4 * q] *= v.x;
-            x[4 * q + 1] *= v.y;
-            x[4 * q + 2] *= v.z;
-            x[4 * q + 3] *= v.w;
-          }
         }
         if (valid < kPage) {  // tokens past the sequence end (or a bad page)
 #pragma unroll
@@ -822,13 +831,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int k = 0; k < 8; ++k) t8[k] = fmaxf(fmaxf(x[k], x[k + 8]), fmaxf(x[k + 16], x[k + 24]));
 #pragma unroll
         for (int k = 0; k < 4; ++k) t8[k] = fmaxf(t8[k], t8[k + 4]);
-        // the row maximum is swapped rounded up to fp16: an upper bound that
-        // both warpgroups share exactly
-        const uint32_t mine = __half_as_ushort(__float2half_ru(fmaxf(fmaxf(t8[0], t8[1]), fmaxf(t8[2], t8[3]))));
-        uint32_t other;
+        const float mine = fmaxf(fmaxf(t8[0], t8[1]), fmaxf(t8[2], t8[3]));
+        float other;
         if (!swap_max(mine, other)) { ok = false; break; }
-        const float mx = fmaxf(__half2float(__ushort_as_half((unsigned short)mine)),
-                               __half2float(__ushort_as_half((unsigned short)other)));
+        const float mx = fmaxf(mine, other);
 
         // online softmax with lazy rescaling: both warpgroups hold the same m
         // and take the same decisions
@@ -899,14 +905,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
 
-      // next unit's query can go in as soon as this unit's last S = Q K^T is done
       Unit nu;
       const bool have_next = wk.next(a, nu);
-      if (have_next) {
-        if (!wwait(B_QFREE, uc & 1)) break;
-        tc_fence_after();
-        load_q(nu);
-      }
 
       // epilogue: the row sum is the two warpgroups' partial sums; each
       // normalises its 128 of this CTA's 256 latent columns

@@ -173,7 +173,8 @@ cudaError_t launch_absorb_tc(const __nv_bfloat16* q_nope, const __nv_bfloat16* w
     return cudaErrorInvalidValue;
   GemmTcArgs g{B, H, N, w_uk, q_lat, 0};
   const size_t smem = 2 * (kABytes + (size_t)N * 128) + 1024;
-  cudaFuncSetAttribute(gemm_tc_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
   dim3 grid(H, kLatent / 128, (B + N - 1) / N);
   gemm_tc_kernel<0><<<grid, 128, smem, stream>>>(tA, tB, g);
   return cudaGetLastError();
@@ -194,7 +195,8 @@ cudaError_t launch_out_proj_tc(const __nv_bfloat16* o_lat, const __nv_bfloat16* 
     return cudaErrorInvalidValue;
   GemmTcArgs g{B, H, N, w_uv, out, out_bf16 ? 2 : 1};
   const size_t smem = 4 * (kABytes + (size_t)N * 128) + 1024;
-  cudaFuncSetAttribute(gemm_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
   dim3 grid(H, 1, (B + N - 1) / N);
   return launch_dependent(gemm_tc_kernel<1>, grid, dim3(128), smem, stream, tA, tB, g);
 }

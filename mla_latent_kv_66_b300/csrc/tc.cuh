@@ -40,6 +40,11 @@ __device__ inline void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// Arrive `count` times at once.
+__device__ inline void mbar_arrive_cnt(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
 __device__ inline void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                : "memory");
@@ -262,10 +267,29 @@ __device__ inline void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t byt
                "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
                : "memory");
 }
-// Arrive on a barrier given by its shared::cluster address (from mapa).
-__device__ inline void mbar_arrive_remote(uint32_t caddr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr)
+// 16-byte load from another CTA's shared memory (address from mapa).
+__device__ inline float4 ld_cluster_v4f(uint32_t caddr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(caddr)
                : "memory");
+  return v;
+}
+// Arrive on a barrier given by its shared::cluster address (from mapa), with
+// the default release semantics at CTA scope: it orders this CTA's earlier
+// reads of shared memory before the arrive (a consumer handing a buffer back
+// to the peer's copy), without waiting for this SM's memory traffic in flight
+// (which a cluster-scope release does, the stage loads included).
+__device__ inline void mbar_arrive_remote(uint32_t caddr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
+}
+// Cluster barrier without release semantics: it does not wait for this
+// CTA's memory operations (loads in flight) to complete.  Used at start-up,
+// where only the barrier initialisation must be visible to the peer, which
+// fence.mbarrier_init already orders.
+__device__ inline void cluster_sync_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 __device__ inline void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" :::

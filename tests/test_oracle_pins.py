@@ -112,6 +112,54 @@ def test_rope_closed_forms_and_invariants():
 
 
 # ---------------------------------------------------------------- attention
+def _rope_score_error(q_rot, k_rot, q_raw, k_raw_rel):
+    """|q_rot . k_rot - q_raw . k_raw_rel| per pair, and the bound that the two
+    bf16 roundings of the rotated vectors allow (half an ulp, 2^-9 relative,
+    on each factor of every product, so 2^-8 on the product, plus slack)."""
+    err = np.abs(np.sum(q_rot * k_rot, axis=-1) - np.sum(q_raw * k_raw_rel, axis=-1))
+    bound = (2.0 ** -8 + 2.0 ** -17) * np.sum(np.abs(q_rot) * np.abs(k_rot), axis=-1) + 1e-12
+    return err, bound
+
+
+def test_query_position_is_the_last_cached_token():
+    """Pin of the reading p_q = n - 1 in rope_q_bf16 (the decoding token's own
+    row is already in the cache).  RoPE depends only on relative position, so
+    the query rotated at p_q and the cached key of token t rotated at t score
+    exactly like the unrotated query against the key rotated by t - p_q.  For
+    the newest token (t = n - 1) that is the unrotated dot product.  Checked
+    for n = 1..130 on 32 query/key pairs each, through the two functions the
+    path uses (rope_q_bf16 for the query, cache_rows_bf16 for the cache);
+    the same check with p_q = n or p_q = 0 fails, so it pins the reading."""
+    rng = np.random.default_rng(17)
+    wrong_n_caught, wrong_0_caught = 0, 0
+    for n in range(1, 131):
+        q_bits = mi.f32_to_bf16_bits(rng.standard_normal((32, 1, 64)).astype(np.float32))
+        k_bits = mi.f32_to_bf16_bits(rng.standard_normal((n, 576)).astype(np.float32))
+        q_rot = O.bf16_to_f64(O.rope_q_bf16(q_bits, np.full(32, n, np.int32)))[:, 0]   # [32,64]
+        k_rot = O.bf16_to_f64(O.cache_rows_bf16(k_bits, np.arange(n))[:, 512:])     # [n,64]
+        q_raw = O.bf16_to_f64(q_bits)[:, 0]
+        k_raw = O.bf16_to_f64(k_bits[:, 512:])
+        # newest token: relative position 0, the unrotated score
+        err, bound = _rope_score_error(q_rot, k_rot[n - 1][None, :], q_raw, k_raw[n - 1][None, :])
+        assert np.all(err <= bound), (n, float(np.max(err / bound)))
+        # every cached token: the key rotated by its offset from the query
+        t = np.arange(n)
+        k_rel = O.rope(k_raw, t - (n - 1))
+        for i in range(0, 32, 8):
+            err, bound = _rope_score_error(q_rot[i][None, :], k_rot, q_raw[i][None, :], k_rel)
+            assert np.all(err <= bound), (n, i)
+        if n > 1:  # the same check rejects the other plausible positions
+            for pos, name in ((n, "n"), (0, "0")):
+                q_wrong = O.bf16_to_f64(O.f64_to_bf16(O.rope(q_raw, pos)))
+                err, bound = _rope_score_error(q_wrong, k_rot[n - 1][None, :], q_raw, k_raw[n - 1][None, :])
+                if np.any(err > bound):
+                    if name == "n":
+                        wrong_n_caught += 1
+                    else:
+                        wrong_0_caught += 1
+    assert wrong_n_caught == 129 and wrong_0_caught == 129
+
+
 def _tiny(B=2, H=4, lens=(65, 130), seed=11, pages="permuted"):
     w = mi.Workload("t", B=B, H=H, L=0, ragged=(1, 2), seed=seed, pages=pages)
     inp = mi.make_inputs(w, with_kv=False)

@@ -61,15 +61,38 @@ def _static(d):
 
 
 def test_static_scratch_matches_the_workspace_entry_point_on_two_calls():
+    """For these batches the fixed scratch holds the automatic partition
+    count, so both entry points run the same kernels on the same schedule
+    and must agree bit for bit; a stale partial from the previous call would
+    show up as a difference.  (The branch that lowers the partition count
+    until the workspace fits is reached only by batches of millions of
+    sequences, and is covered here only by the rejection case below.)"""
     cases = [_inputs([2000, 64, 1, 777, 130], H=128, seed=31),
              _inputs([4096, 3000, 65], H=128, seed=32)]
     for d in cases:
         o_ref, lse_ref = _with_workspace(d)
         o, lse = _static(d)
         torch.cuda.synchronize()
+        assert L.mla_decode_static_status() == L.MLA_OK
+        assert torch.equal(o.view(torch.int16), o_ref.view(torch.int16))
+        assert torch.equal(lse, lse_ref)
         ok, err, bound = tol_ok(to_f64(o), to_f64(o_ref), TOL_REL, TOL_ABS)
         assert ok, (err, bound)
-        assert np.allclose(to_f64(lse), to_f64(lse_ref), rtol=0, atol=1e-3)
+
+
+def test_static_scratch_reports_device_side_errors():
+    """A sequence length outside [1, max_pages*64] is skipped by the kernels
+    and recorded in the scratch's error word, which the status call reads
+    (and clears); the next call starts from a clear word."""
+    d = _inputs([300, 100], H=16, seed=33)
+    bad = dict(d)
+    bad["lens"] = i32_dev(np.array([0, 100], np.int32))
+    _static(bad)
+    assert L.mla_decode_static_status(clear=True) == L.MLA_ERR_SEQ_LEN
+    assert L.mla_decode_static_status() == L.MLA_OK
+    _static(bad)
+    _static(d)  # a good call clears the word when it starts
+    assert L.mla_decode_static_status() == L.MLA_OK
 
 
 def test_static_scratch_rejects_a_batch_too_large_for_it():
