@@ -954,7 +954,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync();  // the peer no longer touches this CTA's shared memory
+  // the peer no longer touches this CTA's shared memory: every copy and
+  // remote arrive it sent here has been waited for by this CTA, so the
+  // barrier need not wait for this CTA's output stores to drain
+  cluster_sync_relaxed();
   if (warp == 2) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
