@@ -307,6 +307,41 @@ def latent_attention_range(cache, page_table, b, t0, t1, q_lat, q_pe):
 
 
 # --------------------------------------------------------------------------
+# several query tokens per sequence (speculative / multi-token decode)
+# --------------------------------------------------------------------------
+def rope_q_multi_bf16(q_pe_raw_bits, seq_lens, q_len) -> np.ndarray:
+    """Rotated key-part of q_len query tokens per sequence, [B,T,H,64] bf16.
+    Reading: the T newest tokens of a sequence of n cached tokens are the
+    queries, token i at position n - T + i (its own row is in the cache)."""
+    q = bf16_to_f64(q_pe_raw_bits)
+    pos = (np.asarray(seq_lens, dtype=np.int64)[:, None] - q_len + np.arange(q_len)[None, :])[:, :, None]
+    return f64_to_bf16(rope(q, pos))
+
+
+def decode_multi_reference(cache, inp, q_pe_rot_bits, q_len, pairs=None):
+    """Non-absorbed decode of q_len query tokens per sequence with a causal
+    mask [P3, forward flow, applied to every new token]: query token i of
+    sequence b (position n - T + i) attends to cache tokens 0..n - T + i.
+    inp["q_nope"] is [B,T,H,128]; q_pe_rot_bits [B,T,H,64].  pairs: list of
+    (b, i, h) (all when None).  Returns (out [len(pairs),128], lse)."""
+    lens, table, w = inp["seq_lens"], inp["page_table"], inp["workload"]
+    if pairs is None:
+        pairs = [(b, i, h) for b in range(len(lens)) for i in range(q_len) for h in range(w.H)]
+    qn, qp = bf16_to_f64(inp["q_nope"]), bf16_to_f64(q_pe_rot_bits)
+    out = np.empty((len(pairs), D_V))
+    lse = np.empty(len(pairs))
+    seq_cache = {}
+    for k, (b, i, h) in enumerate(pairs):
+        if b not in seq_cache:
+            seq_cache = {b: gather_sequence(cache, table, b, int(lens[b]))}
+        c, kp = seq_cache[b]
+        visible = int(lens[b]) - q_len + i + 1
+        out[k], lse[k], _ = decode_head(c[:visible], kp[:visible], qn[b, i, h], qp[b, i, h],
+                                        bf16_to_f64(inp["w_uk"][h]), bf16_to_f64(inp["w_uv"][h]))
+    return out, lse
+
+
+# --------------------------------------------------------------------------
 # cache accounting [P3, cache-size table "每层每 token 缓存"]
 # --------------------------------------------------------------------------
 def cache_accounting(heads=128, d_k=128, d_v=128, layers=60, tokens=131072, bytes_per=2):

@@ -293,6 +293,92 @@ def test_split_ranges_combine_by_lse_to_the_full_result():
     assert math.isclose(m + math.log(w.sum()), lse_full, rel_tol=1e-13)
 
 
+# ---------------------------------------------------------------- several query tokens
+def _multi(lens, T, H=4, seed=13):
+    inp = _tiny(B=len(lens), H=H, lens=lens, seed=seed)
+    rng_q = np.random.default_rng(seed + 100)
+    inp["q_nope"] = mi.f32_to_bf16_bits(rng_q.standard_normal((len(lens), T, H, 128)).astype(np.float32))
+    inp["q_pe_raw"] = mi.f32_to_bf16_bits(rng_q.standard_normal((len(lens), T, H, 64)).astype(np.float32))
+    return inp
+
+
+def test_multi_token_with_one_query_is_the_decode():
+    inp = _multi((65, 130), T=1)
+    cache = O.build_cache(inp)
+    qpe = O.rope_q_multi_bf16(inp["q_pe_raw"], inp["seq_lens"], 1)
+    got, lse = O.decode_multi_reference(cache, inp, qpe, 1)
+    one = dict(inp)
+    one["q_nope"], one["q_pe_raw"] = inp["q_nope"][:, 0], inp["q_pe_raw"][:, 0]
+    ref, lse_ref = O.decode_reference(cache, one, O.rope_q_bf16(one["q_pe_raw"], inp["seq_lens"]))
+    assert np.array_equal(got, ref) and np.array_equal(lse, lse_ref)
+
+
+def test_multi_token_causal_mask_against_a_masked_score_matrix():
+    """Brute force from the whole [T x n] score matrix with -inf above the
+    causal diagonal (query i at position n - T + i), built independently of
+    decode_head: scores against explicitly decompressed keys, masked
+    softmax, weighted decompressed values."""
+    T = 4
+    inp = _multi((5, 70), T=T)
+    cache = O.build_cache(inp)
+    qpe = O.rope_q_multi_bf16(inp["q_pe_raw"], inp["seq_lens"], T)
+    got, _ = O.decode_multi_reference(cache, inp, qpe, T)
+    qn, qp = O.bf16_to_f64(inp["q_nope"]), O.bf16_to_f64(qpe)
+    k = 0
+    for b in range(2):
+        n = int(inp["seq_lens"][b])
+        c, kp = O.gather_sequence(cache, inp["page_table"], b, n)
+        for i in range(T):
+            for h in range(4):
+                wuk, wuv = O.bf16_to_f64(inp["w_uk"][h]), O.bf16_to_f64(inp["w_uv"][h])
+                keys = np.concatenate([c @ wuk.T, kp], axis=1)          # [n,192]
+                s = keys @ np.concatenate([qn[b, i, h], qp[b, i, h]]) / math.sqrt(192)
+                s[np.arange(n) > n - T + i] = -np.inf
+                e = np.exp(s - s.max())
+                ref = (e / e.sum()) @ (c @ wuv.T)
+                assert np.allclose(got[k], ref, rtol=1e-12, atol=1e-13), (b, i, h)
+                k += 1
+
+
+def test_multi_token_outputs_ignore_later_tokens_and_the_last_sees_all():
+    T = 3
+    inp = _multi((67,), T=T)
+    cache = O.build_cache(inp)
+    qpe = O.rope_q_multi_bf16(inp["q_pe_raw"], inp["seq_lens"], T)
+    got, _ = O.decode_multi_reference(cache, inp, qpe, T)
+    # overwrite the rows past query 0's position: query 0's outputs stay bit-exact
+    n = 67
+    moved = {k: (np.array(v, copy=True) if isinstance(v, np.ndarray) else v) for k, v in cache.items()}
+    for t in range(n - T + 1, n):
+        pg, sl = inp["page_table"][0, t // 64], t % 64
+        moved["ckv"][pg, sl] = O.f64_to_bf16(np.full(512, 2.5))
+        moved["kpe"][pg, sl] = O.f64_to_bf16(np.full(64, -1.5))
+    got2, _ = O.decode_multi_reference(moved, inp, qpe, T)
+    assert np.array_equal(got2[:4], got[:4])          # query 0, all heads
+    assert not np.allclose(got2[8:], got[8:])          # the last query sees them
+    # the last query token is the plain decode of the whole sequence
+    one = dict(inp)
+    one["q_nope"] = inp["q_nope"][:, T - 1]
+    ref, _ = O.decode_reference(cache, one, qpe[:, T - 1])
+    assert np.array_equal(got[8:12], ref)
+
+
+def test_multi_token_query_rotation_positions():
+    """Query token i is rotated at n - T + i: against the newest visible key
+    (relative position 0) its RoPE score is the unrotated dot product."""
+    T, n = 3, 40
+    rng = np.random.default_rng(5)
+    q_bits = mi.f32_to_bf16_bits(rng.standard_normal((1, T, 1, 64)).astype(np.float32))
+    k_bits = mi.f32_to_bf16_bits(rng.standard_normal((n, 576)).astype(np.float32))
+    q_rot = O.bf16_to_f64(O.rope_q_multi_bf16(q_bits, np.array([n]), T))[0, :, 0]
+    k_rot = O.bf16_to_f64(O.cache_rows_bf16(k_bits, np.arange(n))[:, 512:])
+    for i in range(T):
+        p = n - T + i
+        err, bound = _rope_score_error(q_rot[i][None], k_rot[p][None], O.bf16_to_f64(q_bits)[0, i, 0][None],
+                                       O.bf16_to_f64(k_bits[p, 512:])[None])
+        assert np.all(err <= bound), i
+
+
 # ---------------------------------------------------------------- cache write
 def test_cache_rows_norm_rope_and_slot_mapping():
     inp = _tiny(B=2, lens=(70, 3))
