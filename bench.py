@@ -185,12 +185,18 @@ def setup_gpu(w, device):
         mla.mla_cache_append(p, bf(mi.kv_rows(w, b, n)), slots,
                              torch.from_numpy(t.astype(np.int32)).to(device), 3, ckv, kpe, sc)
     lens_d = torch.from_numpy(lens).to(device)
-    q_pe = torch.empty(w.B, w.H, 64, dtype=torch.bfloat16, device=device)
-    mla.mla_rope_q(p, bf(inp["q_pe_raw"]), lens_d, q_pe)
-    state = dict(inp=inp, p=p, ckv=ckv, kpe=kpe, sc=sc, lens=lens_d,
-                 table=torch.from_numpy(table).to(device), q_nope=bf(inp["q_nope"]), q_pe=q_pe,
+    table_d = torch.from_numpy(table).to(device)
+    step = mla.MLADecodeStep(w.B, w.H, table.shape[1], npg, w.kv_dtype, w.out_dtype, w.splits, device,
+                             q_len=w.q_len)
+    # rows of the step: the sequences, or q_len rows per sequence (the page
+    # table and lengths the four calls see; the query is rotated at each
+    # row's length minus one)
+    rows_table, rows_lens = step.expand_rows(table_d, lens_d)
+    q_pe = torch.empty(w.B * w.q_len, w.H, 64, dtype=torch.bfloat16, device=device)
+    mla.mla_rope_q(step.p, bf(inp["q_pe_raw"].reshape(-1, w.H, 64)), rows_lens, q_pe)
+    state = dict(inp=inp, p=p, ckv=ckv, kpe=kpe, sc=sc, lens=lens_d, table=table_d,
+                 rows_table=rows_table, rows_lens=rows_lens, q_nope=bf(inp["q_nope"]), q_pe=q_pe,
                  w_uk=bf(inp["w_uk"]), w_uv=bf(inp["w_uv"]))
-    step = mla.MLADecodeStep(w.B, w.H, table.shape[1], npg, w.kv_dtype, w.out_dtype, w.splits, device)
     torch.cuda.synchronize()
     return state, step
 
@@ -231,9 +237,10 @@ def run_ours(args, w, rank, world):
     def one(ev=None):
         L.mla_absorb_q(p, st["q_nope"], st["w_uk"], step.q_lat)
         if ev:
+            torch.cuda._sleep(100000)  # the decode launch is queued before the event fires
             ev[0].record()
-        L.mla_decode(p, step.q_lat, st["q_pe"], st["ckv"], st["kpe"], st["sc"], st["table"], st["lens"], G,
-                     step.workspace, step.o_lat, step.lse)
+        L.mla_decode(p, step.q_lat, st["q_pe"], st["ckv"], st["kpe"], st["sc"], st["rows_table"], st["rows_lens"],
+                     G, step.workspace, step.o_lat, step.lse)
         if ev:
             ev[1].record()
         L.mla_split_kv_combine(p, step.workspace, G, step.o_lat, step.lse)
@@ -367,7 +374,11 @@ class OracleSample:
                "q_nope": self.base["q_nope"][[b]], "q_pe_raw": self.base["q_pe_raw"][[b]],
                "w_uk": self.base["w_uk"], "w_uv": self.base["w_uv"], "kv_raw": {0: mi.kv_rows(w, b, n)}}
         cache = O.build_cache(sub, w.kv_dtype)
-        self.cur = (sub, cache, O.rope_q_bf16(sub["q_pe_raw"], sub["seq_lens"]))
+        if w.q_len > 1:
+            qpe = O.rope_q_multi_bf16(sub["q_pe_raw"], sub["seq_lens"], w.q_len)
+        else:
+            qpe = O.rope_q_bf16(sub["q_pe_raw"], sub["seq_lens"])
+        self.cur = (sub, cache, qpe)
         self.seqs.append((b, n))
 
     def run(self, budget_s):
@@ -379,7 +390,11 @@ class OracleSample:
                 self._load()
             sub, cache, qpe = self.cur
             t0 = time.perf_counter()
-            self.O.decode_reference(cache, sub, qpe, [(0, self.h)])
+            if self.w.q_len > 1:  # one (sequence, head) pair: all of its query tokens
+                self.O.decode_multi_reference(cache, sub, qpe, self.w.q_len,
+                                              [(0, i, self.h) for i in range(self.w.q_len)])
+            else:
+                self.O.decode_reference(cache, sub, qpe, [(0, self.h)])
             spent += time.perf_counter() - t0
             pairs += 1
             self.h += 1
@@ -398,7 +413,7 @@ def cpu_oracle_sample(w, budget_s=15.0, seed=0):
     sequence) over about budget_s seconds; returns (value, threads, text)."""
     s = OracleSample(w, seed)
     pairs, spent = s.run(budget_s)
-    return (pairs / w.H) / spent, blas_threads(), s.describe(pairs, spent)
+    return (pairs * w.q_len / w.H) / spent, blas_threads(), s.describe(pairs, spent)
 
 
 def run_reference(args, w):
@@ -412,7 +427,7 @@ def run_reference(args, w):
     for _ in range(args.steps):
         p, t = s.run(per_step)
         pairs, spent = pairs + p, spent + t
-    return (pairs / w.H) / spent, blas_threads(), s.describe(pairs, spent), 1000.0 * spent / args.steps
+    return (pairs * w.q_len / w.H) / spent, blas_threads(), s.describe(pairs, spent), 1000.0 * spent / args.steps
 
 
 # --------------------------------------------------------------------------- main
@@ -420,7 +435,7 @@ def main():
     args = parse()
     w = mi.WORKLOADS[args.workload]
     rank, world = int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
-    cfg = {"workload": w.name, "B": w.B, "H": w.H, "L": w.L or "log-uniform[%d,%d]" % w.ragged,
+    cfg = {"workload": w.name, "B": w.B, "H": w.H, "L": w.L or "log-uniform[%d,%d]" % w.ragged, "q_len": w.q_len,
            "kv_lora_rank": 512, "rope_dim": 64, "page_size": 64, "kv_dtype": w.kv_dtype,
            "pages": w.pages, "l2": "flushed before every timed step (256 MiB write)",
            "step": "CUDA graph: q absorption, decode, split-KV combine, out-projection",
@@ -450,7 +465,7 @@ def main():
             torch.distributed.destroy_process_group()
         return
     hbm, tflops, src = peaks()
-    tokens_per_step = w.B
+    tokens_per_step = w.B * w.q_len
     value = job_tokens_per_s(world, tokens_per_step, r["ms"])
     cache_bytes = r["tokens"] * cache_bytes_per_token(w.kv_dtype)
     achieved = cache_bytes / (r["dec_ms"] / 1000.0) / 1e9

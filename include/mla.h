@@ -216,6 +216,29 @@ mla_status mla_rope_q(const mla_params* p, const void* q_pe_raw, const int32_t* 
                       void* q_pe, mla_stream_t stream);
 
 /* ---------------------------------------------------------------------
+ * mla_multi_token_expand: several query tokens per sequence (speculative or
+ * multi-token decode, with a causal mask).  The page's forward flow applies
+ * to every new token; with T new tokens the T newest cache positions of a
+ * sequence of n cached tokens are the queries (their rows already in the
+ * cache), token i at position n - T + i, and token i attends to cache
+ * tokens 0 .. n - T + i.  That is the one-token decode of a sequence of
+ * length n - T + 1 + i over the same pages, so this call writes, for the
+ * B sequences of p, B*T rows r = b*T + i:
+ *   page_table_out[r][:] = page_table[b][:]    [B*T, max_pages_per_seq] int32
+ *   seq_lens_out[r]      = seq_lens[b] - T + 1 + i            [B*T] int32
+ * and the caller runs mla_rope_q, mla_absorb_q, mla_decode,
+ * mla_split_kv_combine and mla_out_proj with B*T in place of B, on queries
+ * laid out [B,T,H,...] (= [B*T,H,...]) and these two arrays; the output is
+ * [B,T,H,128].  Requires seq_lens[b] >= T on the device (a shorter sequence
+ * yields a row of length < 1, which mla_decode reports as MLA_ERR_SEQ_LEN).
+ *   q_len : T >= 1;  page_table, seq_lens : as for mla_decode (B rows)
+ *   page_table_out, seq_lens_out : caller-allocated device buffers
+ */
+mla_status mla_multi_token_expand(const mla_params* p, int q_len, const int32_t* page_table,
+                                  const int32_t* seq_lens, int32_t* page_table_out, int32_t* seq_lens_out,
+                                  mla_stream_t stream);
+
+/* ---------------------------------------------------------------------
  * mla_decode_static: mla_decode followed by mla_split_kv_combine, for
  * callers that cannot allocate device memory.  The pages have no counterpart:
  * this is a calling convention, not a step of the method.

@@ -12,8 +12,8 @@ kv_lora_rank 512, qk_rope_head_dim 64, 128 heads of 128 nope + 64 rope, value
 head 128).
 
 Draws (one numpy PCG64 stream per tensor, keyed by the workload seed):
-  q_nope   [B,H,128]  N(0,1)          -> bf16
-  q_pe_raw [B,H,64]   N(0,1) pre-RoPE -> bf16
+  q_nope   [B,H,128]  N(0,1)          -> bf16   ([B,T,H,128] for T query tokens)
+  q_pe_raw [B,H,64]   N(0,1) pre-RoPE -> bf16   ([B,T,H,64])
   w_uk     [H,128,512] N(0,1/512)     -> bf16  (head, nope row, latent)
   w_uv     [H,128,512] N(0,1/512)     -> bf16  (head, value row, latent)
   kv_raw   [T,576]    N(0,1)          -> bf16  one row per cached token, the
@@ -53,6 +53,7 @@ class Workload:
     kv_dtype: str = "bf16"       # bf16 | e4m3
     out_dtype: str = "f32"       # f32 | bf16
     splits: int = 0              # KV partitions to request (0 = automatic)
+    q_len: int = 1               # query tokens per sequence (the newest positions)
 
     @property
     def tokens_hint(self) -> int:
@@ -68,6 +69,8 @@ WORKLOADS = {
                        pages="pool"),
     "fp8_batch": Workload("fp8_batch", B=128, H=128, L=8192, seed=4,
                           kv_dtype="e4m3", out_dtype="bf16"),
+    # two query tokens per sequence (speculative / multi-token decode)
+    "mtp2": Workload("mtp2", B=32, H=128, L=4096, seed=5, q_len=2),
 }
 
 
@@ -125,6 +128,10 @@ def kv_rows(w: Workload, b: int, n: int) -> np.ndarray:
     return _normal_bf16(_rng(w.seed, _S_KV, b), (n, D_ROW))
 
 
+def _qshape(w: Workload, d: int):
+    return (w.B, w.H, d) if w.q_len == 1 else (w.B, w.q_len, w.H, d)
+
+
 def make_inputs(w: Workload, seqs=None, with_kv: bool = True) -> dict:
     """Draw every input of workload ``w``.
 
@@ -138,8 +145,8 @@ def make_inputs(w: Workload, seqs=None, with_kv: bool = True) -> dict:
         "seq_lens": lens,
         "page_table": table,
         "num_pages": num_pages,
-        "q_nope": _normal_bf16(_rng(w.seed, _S_QNOPE), (w.B, w.H, D_NOPE)),
-        "q_pe_raw": _normal_bf16(_rng(w.seed, _S_QPE), (w.B, w.H, D_ROPE)),
+        "q_nope": _normal_bf16(_rng(w.seed, _S_QNOPE), _qshape(w, D_NOPE)),
+        "q_pe_raw": _normal_bf16(_rng(w.seed, _S_QPE), _qshape(w, D_ROPE)),
         "w_uk": _normal_bf16(_rng(w.seed, _S_WUK), (w.H, D_NOPE, D_LATENT), 1.0 / math.sqrt(512.0)),
         "w_uv": _normal_bf16(_rng(w.seed, _S_WUV), (w.H, D_V, D_LATENT), 1.0 / math.sqrt(512.0)),
     }

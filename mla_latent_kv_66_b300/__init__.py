@@ -9,6 +9,7 @@ mla_latent_kv_66_b300.build` compiles it in-tree.
 _BINDINGS = ("MLAError", "MlaParams", "make_params", "mla_absorb_q", "mla_cache_append", "mla_decode",
              "mla_decode_num_splits", "mla_decode_workspace_size", "mla_out_proj", "mla_rope_q",
              "mla_split_kv_combine", "mla_workspace_offsets", "mla_workspace_status", "status_string",
+             "mla_multi_token_expand", "mla_decode_static", "mla_decode_static_status",
              "MLA_APPEND_RMSNORM", "MLA_APPEND_ROPE", "LIB_PATH")
 
 

@@ -61,6 +61,7 @@ _SIGS = {
                                         _P, _P, _P, _P]),
     "mla_rope_q": (ctypes.c_int, [ctypes.POINTER(MlaParams), _P, _P, _P, _P]),
     "mla_workspace_status": (ctypes.c_int, [_P, ctypes.c_int, _P]),
+    "mla_multi_token_expand": (ctypes.c_int, [ctypes.POINTER(MlaParams), ctypes.c_int, _P, _P, _P, _P, _P]),
     "mla_decode_static": (ctypes.c_int, [ctypes.POINTER(MlaParams), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "mla_decode_static_status": (ctypes.c_int, [ctypes.c_int, _P]),
 }
@@ -169,3 +170,10 @@ def mla_decode_static(p, q_lat, q_pe, ckv, kpe, kv_scale, page_table, seq_lens, 
 def mla_decode_static_status(clear=False, stream=None) -> int:
     """Error word of mla_decode_static's fixed scratch (synchronises the stream)."""
     return lib.mla_decode_static_status(1 if clear else 0, _stream(stream))
+
+
+def mla_multi_token_expand(p, q_len, page_table, seq_lens, page_table_out, seq_lens_out, stream=None):
+    """Rows b*q_len + i of the causal multi-token decode: page-table row b and
+    length seq_lens[b] - q_len + 1 + i (p.B = number of sequences)."""
+    _check(lib.mla_multi_token_expand(ctypes.byref(p), q_len, _ptr(page_table), _ptr(seq_lens), _ptr(page_table_out),
+                                      _ptr(seq_lens_out), _stream(stream)), "mla_multi_token_expand")

@@ -214,6 +214,18 @@ mla_status mla_rope_q(const mla_params* p, const void* q_pe_raw, const int32_t* 
                                    (cudaStream_t)stream));
 }
 
+mla_status mla_multi_token_expand(const mla_params* p, int q_len, const int32_t* page_table,
+                                  const int32_t* seq_lens, int32_t* page_table_out, int32_t* seq_lens_out,
+                                  mla_stream_t stream) {
+  mla_status s = check_params(p);
+  if (s != MLA_OK) return s;
+  if (q_len < 1 || !page_table || !seq_lens || !page_table_out || !seq_lens_out) return MLA_ERR_INVALID_ARG;
+  if ((long long)p->B * q_len > 0x7fffffffLL || (long long)p->B * q_len * p->max_pages_per_seq > 0x7fffffffLL)
+    return MLA_ERR_UNSUPPORTED;
+  return cuda_status(launch_multi_token_expand(page_table, seq_lens, p->B, q_len, p->max_pages_per_seq,
+                                               page_table_out, seq_lens_out, (cudaStream_t)stream));
+}
+
 mla_status mla_workspace_status(void* workspace, int clear, mla_stream_t stream) {
   if (!workspace) return MLA_ERR_INVALID_ARG;
   int v = 0;

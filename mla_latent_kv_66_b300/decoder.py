@@ -11,27 +11,51 @@ from . import _lib as L
 
 
 class MLADecodeStep:
+    """q_len > 1: that many query tokens per sequence (the newest cache
+    positions, causal); queries are [B,q_len,H,...] and the output
+    [B,q_len,H,128].  The page table and lengths passed to a call are the B
+    sequences'; the step expands them into B*q_len rows (expand_rows), whose
+    lengths are also what mla_rope_q needs to rotate the queries."""
+
     def __init__(self, B, H, max_pages_per_seq, num_pages, kv_dtype="bf16", out_dtype="f32",
-                 num_splits=0, device="cuda"):
-        self.p = L.make_params(B, H, max_pages_per_seq, num_pages, kv_dtype, out_dtype)
+                 num_splits=0, device="cuda", q_len=1):
+        rows = B * q_len
+        self.q_len = q_len
+        self.p_seq = L.make_params(B, H, max_pages_per_seq, num_pages, kv_dtype, out_dtype)
+        self.p = L.make_params(rows, H, max_pages_per_seq, num_pages, kv_dtype, out_dtype)
         self.num_splits = L.mla_decode_num_splits(self.p, num_splits)
         if self.num_splits < 1:
             raise L.MLAError(L.MLA_ERR_INVALID_ARG, "MLADecodeStep")
         ws = L.mla_decode_workspace_size(self.p, self.num_splits)
         self.workspace = torch.zeros(ws, dtype=torch.uint8, device=device)
-        self.q_lat = torch.empty(B, H, 512, dtype=torch.bfloat16, device=device)
-        self.o_lat = torch.empty(B, H, 512, dtype=torch.bfloat16, device=device)
-        self.lse = torch.empty(B, H, dtype=torch.float32, device=device)
+        self.q_lat = torch.empty(rows, H, 512, dtype=torch.bfloat16, device=device)
+        self.o_lat = torch.empty(rows, H, 512, dtype=torch.bfloat16, device=device)
+        self.lse = torch.empty(rows, H, dtype=torch.float32, device=device)
         odt = torch.bfloat16 if out_dtype == "bf16" else torch.float32
-        self.out = torch.empty(B, H, 128, dtype=odt, device=device)
+        self.out = torch.empty(rows, H, 128, dtype=odt, device=device)
+        if q_len > 1:
+            self.table_rows = torch.empty(rows, max_pages_per_seq, dtype=torch.int32, device=device)
+            self.lens_rows = torch.empty(rows, dtype=torch.int32, device=device)
+
+    def expand_rows(self, page_table, seq_lens, stream=None):
+        """Page table and lengths of the B*q_len rows (the inputs themselves
+        when q_len == 1)."""
+        if self.q_len == 1:
+            return page_table, seq_lens
+        L.mla_multi_token_expand(self.p_seq, self.q_len, page_table, seq_lens, self.table_rows, self.lens_rows,
+                                 stream)
+        return self.table_rows, self.lens_rows
 
     def __call__(self, q_nope, q_pe, w_uk, w_uv, ckv, kpe, kv_scale, page_table, seq_lens, stream=None):
         p, G = self.p, self.num_splits
+        page_table, seq_lens = self.expand_rows(page_table, seq_lens, stream)
         L.mla_absorb_q(p, q_nope, w_uk, self.q_lat, stream)
         L.mla_decode(p, self.q_lat, q_pe, ckv, kpe, kv_scale, page_table, seq_lens, G,
                      self.workspace, self.o_lat, self.lse, stream)
         L.mla_split_kv_combine(p, self.workspace, G, self.o_lat, self.lse, stream)
         L.mla_out_proj(p, self.o_lat, w_uv, self.out, stream)
+        if self.q_len > 1:
+            return self.out.view(-1, self.q_len, *self.out.shape[1:])
         return self.out
 
     def capture(self, *inputs):
@@ -50,6 +74,8 @@ class MLADecodeStep:
 
     def replay(self):
         self.graph.replay()
+        if self.q_len > 1:
+            return self.out.view(-1, self.q_len, *self.out.shape[1:])
         return self.out
 
     def status(self, clear=False):

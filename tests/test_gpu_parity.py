@@ -391,6 +391,81 @@ def test_fp8_encoder_on_every_finite_bf16_pattern():
                           O.f32_to_e4m3(O.bf16_to_f64(in_range).astype(np.float32)))
 
 
+# ------------------------------------------------------------------ several query tokens per sequence
+def multi_inputs(lens, T, H=16, seed=27):
+    w = mi.Workload("m", B=len(lens), H=H, L=0, ragged=(1, 2), seed=seed, pages="permuted", q_len=T)
+    inp = mi.make_inputs(w, with_kv=False)
+    inp["seq_lens"] = np.asarray(lens, np.int32)
+    inp["page_table"], inp["num_pages"] = mi.page_layout(w, inp["seq_lens"])
+    inp["kv_raw"] = {b: mi.kv_rows(w, b, int(lens[b])) for b in range(len(lens))}
+    return inp
+
+
+def run_multi(inp, cache, q_pe_bits, T, num_splits=0):
+    B, H = len(inp["seq_lens"]), inp["workload"].H
+    table = inp["page_table"]
+    step = mla.MLADecodeStep(B, H, table.shape[1], inp["num_pages"], cache["kv_dtype"], num_splits=num_splits,
+                             q_len=T)
+    ckv, kpe, sc = upload_cache(cache)
+    out = step(bf16_dev(inp["q_nope"]), bf16_dev(q_pe_bits), bf16_dev(inp["w_uk"]), bf16_dev(inp["w_uv"]),
+               ckv, kpe, sc, i32_dev(table), i32_dev(inp["seq_lens"]))
+    torch.cuda.synchronize()
+    return step, out
+
+
+def test_multi_token_decode_against_the_oracle():
+    """Three query tokens per sequence with a causal mask, through the row
+    expansion and the four calls: every (sequence, token, head) against the
+    oracle, including a sequence exactly as long as the query block; the
+    expanded page table and lengths bit-exact; the GPU query rotation at the
+    expanded lengths within one bf16 ulp of the oracle's."""
+    T = 3
+    lens = [3, 70, 200, 64]
+    inp = multi_inputs(lens, T)
+    cache = O.build_cache(inp, garbage=garbage(inp))
+    qpe = O.rope_q_multi_bf16(inp["q_pe_raw"], inp["seq_lens"], T)
+    for splits in (0, 5):
+        step, out = run_multi(inp, cache, qpe, T, splits)
+        assert step.status() == 0
+        ref, _ = O.decode_multi_reference(cache, inp, qpe, T)
+        got = to_f64(out).reshape(-1, 128)
+        ok, err, bound = tol_ok(got, ref, TOL_REL, TOL_ABS)
+        assert ok, (splits, err, bound)
+        # the LSE against the absorbed attention on the GPU's own q_lat, over
+        # each row's visible tokens (a one-token row's LSE is a single score,
+        # so the bf16 rounding of q_lat would dominate a comparison with the
+        # non-absorbed oracle)
+        ql, qp = to_f64(step.q_lat).reshape(len(lens), T, 16, 512), O.bf16_to_f64(qpe)
+        glse = to_f64(step.lse).reshape(len(lens), T, 16)
+        for b, n in enumerate(lens):
+            c, kp = O.gather_sequence(cache, inp["page_table"], b, n)
+            for i in range(T):
+                vis = n - T + 1 + i
+                for h in range(16):
+                    _, lse_ref = O.latent_attention(c[:vis], kp[:vis], ql[b, i, h], qp[b, i, h])
+                    assert abs(glse[b, i, h] - lse_ref) < 1e-3, (splits, b, i, h)
+    table, rows_lens = step.table_rows.cpu().numpy(), step.lens_rows.cpu().numpy()
+    assert np.array_equal(table, np.repeat(inp["page_table"], T, axis=0))
+    assert np.array_equal(rows_lens, np.array([n - T + 1 + i for n in lens for i in range(T)], np.int32))
+    p = L.make_params(len(lens) * T, 16, inp["page_table"].shape[1], inp["num_pages"])
+    q = torch.empty(len(lens) * T, 16, 64, dtype=torch.bfloat16, device="cuda")
+    L.mla_rope_q(p, bf16_dev(inp["q_pe_raw"].reshape(-1, 16, 64)), step.lens_rows, q)
+    d = np.abs(bf16_bits(q).astype(np.int32) - qpe.reshape(-1, 16, 64).astype(np.int32))
+    assert d.max() <= 1 and np.mean(d == 0) > 0.999
+
+
+def test_multi_token_sequence_shorter_than_the_query_block_is_reported():
+    T = 4
+    inp = multi_inputs([2, 100], T)
+    cache = O.build_cache(inp)
+    qpe = O.rope_q_multi_bf16(inp["q_pe_raw"], np.maximum(inp["seq_lens"], T), T)
+    step, out = run_multi(inp, cache, qpe, T)
+    assert step.status() == L.MLA_ERR_SEQ_LEN
+    # the valid sequence is still decoded correctly
+    ref, _ = O.decode_multi_reference(cache, inp, qpe, T, [(1, i, h) for i in range(T) for h in range(16)])
+    assert tol_ok(to_f64(out[1]).reshape(-1, 128), ref, TOL_REL, TOL_ABS)[0]
+
+
 # ------------------------------------------------------------------ full-size workloads, sampled
 def build_gpu_cache(inp, kv_dtype):
     """Write the whole workload's cache with the GPU append kernel."""
@@ -436,6 +511,48 @@ def oracle_sampled(w, pairs, kv_dtype=None):
     cache = O.build_cache(sub, kv_dtype or w.kv_dtype)
     qpe = O.rope_q_bf16(sub["q_pe_raw"], sub["seq_lens"])
     return O.decode_reference(cache, sub, qpe, [(seqs.index(b), h) for b, h in pairs])
+
+
+def test_full_size_multi_token_sampled():
+    """Two query tokens per sequence at the DeepSeek-V2 layer shape (B=32,
+    H=128, L=4096): sampled (sequence, token, head) triples against the
+    oracle, which computes each one by one."""
+    w = mi.WORKLOADS["mtp2"]
+    T = w.q_len
+    inp = mi.make_inputs(w, with_kv=False)
+    ckv, kpe, sc = build_gpu_cache(inp, w.kv_dtype)
+    table = inp["page_table"]
+    step = mla.MLADecodeStep(w.B, w.H, table.shape[1], inp["num_pages"], q_len=T)
+    lens = i32_dev(inp["seq_lens"])
+    tab = i32_dev(table)
+    rows_table, rows_lens = step.expand_rows(tab, lens)
+    p = L.make_params(w.B * T, w.H, table.shape[1], inp["num_pages"])
+    qpe = torch.empty(w.B * T, w.H, 64, dtype=torch.bfloat16, device="cuda")
+    L.mla_rope_q(p, bf16_dev(inp["q_pe_raw"].reshape(-1, w.H, 64)), rows_lens, qpe)
+    out = step(bf16_dev(inp["q_nope"]), qpe, bf16_dev(inp["w_uk"]), bf16_dev(inp["w_uv"]), ckv, kpe, sc, tab, lens)
+    torch.cuda.synchronize()
+    assert step.status() == 0
+    rng = np.random.default_rng(w.seed)
+    triples = [(int(b), int(i), int(h)) for b in sorted(rng.choice(w.B, 3, replace=False))
+               for i in range(T) for h in sorted(rng.choice(w.H, 2, replace=False))]
+    seqs = sorted({b for b, _, _ in triples})
+    full = mi.make_inputs(w, seqs=seqs)
+    npg = (full["seq_lens"][seqs] + 63) // 64
+    sub_table = np.full((len(seqs), int(npg.max())), -1, np.int32)
+    k = 0
+    for r_, n in enumerate(npg):
+        sub_table[r_, :n] = np.arange(k, k + n)
+        k += int(n)
+    sub = {"workload": dataclasses.replace(w, B=len(seqs)), "seq_lens": full["seq_lens"][seqs],
+           "page_table": sub_table, "num_pages": k, "q_nope": full["q_nope"][seqs],
+           "q_pe_raw": full["q_pe_raw"][seqs], "w_uk": full["w_uk"], "w_uv": full["w_uv"],
+           "kv_raw": {r_: full["kv_raw"][b] for r_, b in enumerate(seqs)}}
+    cache = O.build_cache(sub)
+    ref, _ = O.decode_multi_reference(cache, sub, O.rope_q_multi_bf16(sub["q_pe_raw"], sub["seq_lens"], T), T,
+                                      [(seqs.index(b), i, h) for b, i, h in triples])
+    got = np.stack([to_f64(out[b, i, h]) for b, i, h in triples])
+    ok, err, bound = tol_ok(got, ref, TOL_REL, TOL_ABS)
+    assert ok, (err, bound)
 
 
 @pytest.mark.parametrize("name,n_seq,n_head", [("v2_layer", 3, 3), ("long_ctx", 1, 3),
