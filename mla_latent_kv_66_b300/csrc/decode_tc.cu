@@ -634,10 +634,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint4 v = ld_shared_v4u(raw + box * 8192 + row * 128 + cc * 16);
         const int col = box * 128 + cc * 16, kb = col >> 6, cb = (col & 63) >> 3;
         const uint32_t rowa = st + kb * kBox + row * 128;
-        st_shared_v4(rowa + ((cb ^ (row & 7)) << 4), e4m3x2_to_bf16x2(v.x), e4m3x2_to_bf16x2(v.x >> 16),
-                     e4m3x2_to_bf16x2(v.y), e4m3x2_to_bf16x2(v.y >> 16));
-        st_shared_v4(rowa + (((cb + 1) ^ (row & 7)) << 4), e4m3x2_to_bf16x2(v.z), e4m3x2_to_bf16x2(v.z >> 16),
-                     e4m3x2_to_bf16x2(v.w), e4m3x2_to_bf16x2(v.w >> 16));
+        // Each 8-lane quarter of the warp expands one row: 4 lanes into box kb
+        // = 2 box, 4 into box 2 box + 1, chunks (cb, cb + 1) each.  The lanes
+        // of the odd box store their second chunk first, so that each store
+        // instruction's quarter touches all 8 bank groups of the row (the
+        // swizzle is the same in both boxes).
+        const uint32_t lo_first = kb & 1;
+        const uint32_t c0 = rowa + (((cb + lo_first) ^ (row & 7)) << 4), c1 = rowa + (((cb + 1 - lo_first) ^ (row & 7)) << 4);
+        const uint32_t e0 = e4m3x2_to_bf16x2(v.x), e1 = e4m3x2_to_bf16x2(v.x >> 16), e2 = e4m3x2_to_bf16x2(v.y),
+                       e3 = e4m3x2_to_bf16x2(v.y >> 16), e4 = e4m3x2_to_bf16x2(v.z), e5 = e4m3x2_to_bf16x2(v.z >> 16),
+                       e6 = e4m3x2_to_bf16x2(v.w), e7 = e4m3x2_to_bf16x2(v.w >> 16);
+        if (lo_first) {
+          st_shared_v4(c0, e4, e5, e6, e7);
+          st_shared_v4(c1, e0, e1, e2, e3);
+        } else {
+          st_shared_v4(c0, e0, e1, e2, e3);
+          st_shared_v4(c1, e4, e5, e6, e7);
+        }
       }
       {  // this CTA's 32 rope codes per token: 64 rows x 2 chunks of 16, into the
          // 64-byte-swizzled k_pe box (16-byte chunk c of row r at c ^ ((r >> 1) & 3))

@@ -10,6 +10,8 @@
 // weights stream once through a TMA pipeline into 128-byte-swizzled shared
 // memory, the accumulator lives in tensor memory.  W_UK is read with its
 // latent axis as M, i.e. as an MN-major A operand; W_UV is K-major.
+#include <algorithm>
+
 #include "kernels.h"
 #include "tc.cuh"
 #include "tmap.cuh"
@@ -23,19 +25,22 @@ constexpr uint32_t kABytes = 16384;  // A bytes per 64-wide K block
 
 struct GemmTcArgs {
   int B, H, N;
+  int S;                        // pipeline stages (K blocks in flight), at most kMaxS
   const __nv_bfloat16* weight;  // [H,128,512]: prefetched into L2 before the dependency wait
   void* out;
   int out_kind;  // 0: q_lat bf16 [B,H,512]; 1: out fp32 [B,H,128]; 2: out bf16 [B,H,128]
 };
+
+constexpr int kMaxS = 8;
 
 template <int kMode>
 __global__ void __launch_bounds__(128, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__ CUtensorMap tB,
                    GemmTcArgs g) {
   constexpr int KB = kMode == 0 ? 2 : 8;  // K blocks of 64
-  constexpr int S = kMode == 0 ? 2 : 4;   // pipeline stages
+  const int S = g.S;                      // pipeline stages
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bars[2 * S + 1];
+  __shared__ __align__(8) uint64_t bars[2 * kMaxS + 1];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -44,7 +49,7 @@ __global__ void __launch_bounds__(128, 1)
   const uint32_t stage = kABytes + b_bytes;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.x, mt = blockIdx.y, nt = blockIdx.z;
-  const uint32_t full = smem_u32(&bars[0]), empty = smem_u32(&bars[S]), done = smem_u32(&bars[2 * S]);
+  const uint32_t full = smem_u32(&bars[0]), empty = smem_u32(&bars[kMaxS]), done = smem_u32(&bars[2 * kMaxS]);
   const uint32_t ncols = g.N <= 32 ? 32 : g.N <= 64 ? 64 : g.N <= 128 ? 128 : 256;
 
   // q absorption opens a decode step: the decode kernel may launch at once.
@@ -171,7 +176,7 @@ cudaError_t launch_absorb_tc(const __nv_bfloat16* q_nope, const __nv_bfloat16* w
   if (!make_tmap(&tA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w_uk, ad, as, abox) ||
       !make_tmap(&tB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q_nope, bd, bs, bbox))
     return cudaErrorInvalidValue;
-  GemmTcArgs g{B, H, N, w_uk, q_lat, 0};
+  GemmTcArgs g{B, H, N, 2, w_uk, q_lat, 0};
   const size_t smem = 2 * (kABytes + (size_t)N * 128) + 1024;
   cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -193,8 +198,12 @@ cudaError_t launch_out_proj_tc(const __nv_bfloat16* o_lat, const __nv_bfloat16* 
   if (!make_tmap(&tA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w_uv, ad, as, abox) ||
       !make_tmap(&tB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, o_lat, bd, bs, bbox))
     return cudaErrorInvalidValue;
-  GemmTcArgs g{B, H, N, w_uv, out, out_bf16 ? 2 : 1};
-  const size_t smem = 4 * (kABytes + (size_t)N * 128) + 1024;
+  // as many of the 8 K blocks in flight as shared memory holds (all 8 for
+  // batches up to 112): the weight slice streams in one go
+  const size_t stage = kABytes + (size_t)N * 128;
+  const int S = (int)std::min<size_t>(kMaxS, (200u << 10) / stage);
+  GemmTcArgs g{B, H, N, S, w_uv, out, out_bf16 ? 2 : 1};
+  const size_t smem = S * stage + 1024;
   cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(H, 1, (B + N - 1) / N);
