@@ -159,6 +159,42 @@ def quantize_rows_e4m3(rows_bf16_bits):
     return f32_to_e4m3(q), scale
 
 
+def quantize_query_e4m3(q_lat_bits, q_pe_bits, terms=2):
+    """Query of the 8-bit tensor-core decode: each (b, h) row of its 576
+    values (the 512 latent ones, then the 64 rotated RoPE ones) as E4M3
+    codes under one fp32 scale.
+
+    [P1, hotdry "DeepSeek-V3.2-Exp 中多头潜在注意力的优化", deployment
+    paragraph: FP8 quantisation when serving MLA.]  The page names no
+    format; the reading mirrors the cache's per-token rule:
+        scale = fp32(max |v|) / 448 in fp32 (1 for an all-zero row)
+        y     = fp32(v) / scale in fp32
+        hi    = E4M3(y)
+        lo    = E4M3(fp32(y - value(hi)))      (terms == 2 only)
+    so that v ~ scale * (value(hi) + value(lo)).  y - value(hi) is exact in
+    fp32 (hi is y rounded to 4 significant bits).  All decisions are taken in
+    fp32, as a kernel takes them.
+    Returns codes uint8 [B, H, terms, 576] and scale float32 [B, H]."""
+    v = np.concatenate([bf16_to_f64(q_lat_bits), bf16_to_f64(q_pe_bits)], axis=-1).astype(np.float32)
+    amax = np.max(np.abs(v), axis=-1)
+    scale = (amax / np.float32(E4M3_MAX)).astype(np.float32)
+    scale = np.where(amax == 0, np.float32(1.0), scale).astype(np.float32)
+    y = (v / scale[..., None]).astype(np.float32)
+    hi = f32_to_e4m3(y)
+    codes = [hi]
+    if terms == 2:
+        r = (y - e4m3_to_f64(hi).astype(np.float32)).astype(np.float32)
+        codes.append(f32_to_e4m3(r))
+    return np.stack(codes, axis=-2), scale
+
+
+def dequantize_query(codes, scale):
+    """fp64 value of an E4M3 query (see quantize_query_e4m3): q_lat [..., 512]
+    and q_pe [..., 64] = scale * sum of the terms' values."""
+    v = np.sum(e4m3_to_f64(codes), axis=-2) * np.asarray(scale, dtype=np.float64)[..., None]
+    return v[..., :D_LATENT], v[..., D_LATENT:]
+
+
 def rope_q_bf16(q_pe_raw_bits, seq_lens) -> np.ndarray:
     """Rotated query key-part [B,H,64] in bf16.  Reading: the decoding token is
     the last cached position, p_q = seq_len - 1 (its own row is in the cache)."""

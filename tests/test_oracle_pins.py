@@ -414,6 +414,63 @@ def test_e4m3_row_quantisation_error_bound():
     assert s[0] == 1.0 and not z.any()
 
 
+def _bf16_bits(x):
+    return O.f64_to_bf16(np.asarray(x, dtype=np.float64))
+
+
+def test_query_quantisation_worked_row():
+    # max |v| = 3.5 -> scale = 3.5/448 = 2^-7 exactly, y = 128 v exactly
+    lat = np.zeros(512)
+    lat[:4] = [3.5, -1.75, 0.1015625, 0.10546875]
+    codes, scale = O.quantize_query_e4m3(_bf16_bits(lat)[None, None], _bf16_bits(np.zeros(64))[None, None])
+    assert scale.shape == (1, 1) and scale[0, 0] == np.float32(2.0 ** -7)
+    hi, lo = codes[0, 0, 0], codes[0, 0, 1]
+    # 448 -> 0x7E; -224 = -1.75 * 2^7 -> 0xF6; 13 = 1.625 * 2^3 -> 0x55 (exact)
+    # 13.5 = 1.6875 * 2^3 lies halfway between 13 (odd code 0x55) and 14 (even
+    # code 0x56): ties to even gives 14 and leaves -0.5 (0xB0) for the second term
+    assert list(hi[:4]) == [0x7E, 0xF6, 0x55, 0x56]
+    assert list(lo[:4]) == [0x00, 0x00, 0x00, 0xB0]
+    assert not hi[4:].any() and not lo[4:].any()
+    one, _ = O.quantize_query_e4m3(_bf16_bits(lat)[None, None], _bf16_bits(np.zeros(64))[None, None], terms=1)
+    assert one.shape == (1, 1, 1, 576) and np.array_equal(one[0, 0, 0], hi)
+
+
+def test_query_quantisation_error_bounds_and_scale_over_all_576():
+    rng = np.random.default_rng(5)
+    B, H = 3, 16
+    lat = rng.standard_normal((B, H, 512)) * np.exp(rng.uniform(-3, 3, (B, H, 1)))
+    pe = rng.standard_normal((B, H, 64)) * np.exp(rng.uniform(-3, 3, (B, H, 1)))
+    pe[0, 0, 7] = 1e3  # this row's maximum sits in the RoPE part
+    lb, pb = _bf16_bits(lat), _bf16_bits(pe)
+    v = np.concatenate([O.bf16_to_f64(lb), O.bf16_to_f64(pb)], -1)
+    for terms, rel in ((2, 2.0 ** -8), (1, 2.0 ** -4)):
+        codes, scale = O.quantize_query_e4m3(lb, pb, terms)
+        assert codes.shape == (B, H, terms, 576)
+        s = scale.astype(np.float64)[..., None]
+        ql, qp = O.dequantize_query(codes, scale)
+        err = np.abs(np.concatenate([ql, qp], -1) - v)
+        # two terms: the second term's own rounding, 2^-4 of a value at most
+        # 2^-4 of |y|; subnormal steps 2^-9 (half: 2^-10) in units of the scale
+        assert np.all(err <= np.maximum(rel * np.abs(v), 2.0 ** -10 * s) * (1 + 1e-6))
+        # the row maximum maps to +-448 and its second term is (signed) zero
+        i = np.argmax(np.abs(v), -1)
+        top = np.take_along_axis(codes[:, :, 0], i[..., None], -1)[..., 0]
+        assert np.all(top & 0x7F == 0x7E)
+        if terms == 2:
+            assert not (np.take_along_axis(codes[:, :, 1], i[..., None], -1) & 0x7F).any()
+    assert np.argmax(np.abs(v[0, 0])) == 512 + 7
+    # second term: every code is an E4M3 rounding of the first term's residual
+    # (quotient and residual formed in fp32 by torch)
+    codes, scale = O.quantize_query_e4m3(lb, pb)
+    y = torch.from_numpy(v.astype(np.float32)) / torch.from_numpy(scale)[..., None]
+    assert np.array_equal(codes[:, :, 0], y.to(torch.float8_e4m3fn).view(torch.uint8).numpy())
+    res = y - torch.from_numpy(O.e4m3_to_f64(codes[:, :, 0]).astype(np.float32))
+    assert np.array_equal(codes[:, :, 1], res.to(torch.float8_e4m3fn).view(torch.uint8).numpy())
+    # zero rows: scale 1, all codes zero
+    z, zs = O.quantize_query_e4m3(np.zeros((1, 1, 512), np.uint16), np.zeros((1, 1, 64), np.uint16))
+    assert zs[0, 0] == 1.0 and not z.any()
+
+
 # ---------------------------------------------------------------- accounting
 def test_cache_accounting_against_page_table():
     g = json.load(open(os.path.join(GOLDEN, "p3_cache_table.json")))
