@@ -20,6 +20,8 @@
  * Conventions for every call:
  *  - All tensors are dense, row-major, contiguous, in device memory unless
  *    a comment says "host".  The caller owns every buffer and the stream.
+ *    mla_decode and mla_split_kv_combine want every tensor and the
+ *    workspace 16-byte aligned (MLA_ERR_INVALID_ARG otherwise).
  *  - No call allocates memory or synchronises, except mla_workspace_status
  *    and mla_decode_static_status, which read one word back.  Calls only
  *    enqueue work on `stream`.
@@ -55,7 +57,29 @@ typedef enum {
   MLA_ERR_TIMEOUT = 7       /* a kernel gave up a bounded wait (internal fault) */
 } mla_status;
 
-typedef enum { MLA_KV_BF16 = 0, MLA_KV_E4M3 = 1 } mla_kv_dtype;
+/* Storage of the latent cache and the arithmetic of mla_decode.
+ *  MLA_KV_BF16       bf16 cache, bf16 tensor-core products.
+ *  MLA_KV_E4M3       E4M3 cache + fp32 scale per token; the codes are
+ *                    expanded exactly to bf16 and multiplied in bf16.
+ *  MLA_KV_E4M3_MMA   the same E4M3 cache multiplied as codes on the 8-bit
+ *                    tensor cores (tcgen05 kind::f8f6f4): mla_decode turns
+ *                    the query into two E4M3 terms under one fp32 scale per
+ *                    head row (see mla_workspace_query_offsets) and the
+ *                    probabilities into two E4M3 terms per P . V product, so
+ *                    each product carries about 8 significant bits more
+ *                    than one E4M3 value.  The cache is never expanded.
+ *  MLA_KV_E4M3_MMA1  as MLA_KV_E4M3_MMA with one E4M3 term for the query
+ *                    and for the probabilities (fewer products, the query's
+ *                    and the probabilities' own E4M3 rounding in the
+ *                    result).
+ * The three E4M3 values share one cache layout (mla_cache_append writes it
+ * for any of them). */
+typedef enum {
+  MLA_KV_BF16 = 0,
+  MLA_KV_E4M3 = 1,
+  MLA_KV_E4M3_MMA = 2,
+  MLA_KV_E4M3_MMA1 = 3
+} mla_kv_dtype;
 typedef enum { MLA_OUT_F32 = 0, MLA_OUT_BF16 = 1 } mla_out_dtype;
 
 /* Problem description shared by every call.  The head dimensions are those of
@@ -126,6 +150,19 @@ int mla_decode_num_splits(const mla_params* p, int num_splits);
 size_t mla_decode_workspace_size(const mla_params* p, int num_splits);
 void mla_workspace_offsets(const mla_params* p, int num_splits, size_t offsets[5]);
 
+/* MLA_KV_E4M3_MMA / _MMA1 only: where mla_decode keeps the E4M3 query in the
+ * workspace (offsets[0], offsets[1]; both 0 for the other kv_dtypes):
+ *   codes [B,H,2,576] uint8 at offsets[0]: per (b,h) row, term 0 then term 1
+ *         (term 1 unused by _MMA1), each 512 latent codes then 64 RoPE codes
+ *   scale [B,H] fp32 at offsets[1]
+ * Row v = [q_lat[b,h] ; q_pe[b,h]] (576 bf16 values): scale = max|v| / 448
+ * (1 for an all-zero row), y = v / scale, term0 = E4M3(y),
+ * term1 = E4M3(y - value(term0)); fp32 divisions, round to nearest even,
+ * saturating.  The page (hotdry.top, "DeepSeek-V3.2-Exp 中多头潜在注意力
+ * 的优化", deployment paragraph) asks for FP8 when serving MLA and names no
+ * format; this mirrors the cache's per-token rule. */
+void mla_workspace_query_offsets(const mla_params* p, int num_splits, size_t offsets[2]);
+
 /* ---------------------------------------------------------------------
  * mla_decode: latent attention of one query token per sequence over its
  * paged cache.  For each (b,h), with n = seq_lens[b] and cached token t in
@@ -138,7 +175,8 @@ void mla_workspace_offsets(const mla_params* p, int num_splits, size_t offsets[5
  * (decode of the newest token, whose own row is already in the cache).
  *   q_lat      : [B,H,512] bf16 (from mla_absorb_q)
  *   q_pe       : [B,H,64] bf16, already rotated at position n-1
- *   ckv_cache  : [num_pages,64,512] bf16, or E4M3 bytes for MLA_KV_E4M3
+ *   ckv_cache  : [num_pages,64,512] bf16, or E4M3 bytes (the MLA_KV_E4M3*
+ *                kv_dtypes)
  *   kpe_cache  : [num_pages,64,64]  bf16, or E4M3 bytes, rotated keys
  *   kv_scale   : [num_pages,64] fp32 per-token dequantisation scale for
  *                E4M3 (value = code * scale); NULL for bf16
@@ -150,6 +188,8 @@ void mla_workspace_offsets(const mla_params* p, int num_splits, size_t offsets[5
  *   lse        : [B,H] fp32 natural-log LSE, written for sequences not split
  *                (may be NULL)
  * Slots past n in a sequence's last page are ignored and may hold anything.
+ * MLA_KV_E4M3_MMA / _MMA1 launch two kernels: the query quantisation into
+ * the workspace, then the decode.
  * Device-side faults of the inputs: a page id outside [0,num_pages) sets
  * MLA_ERR_PAGE_OOB and that page's tokens are left out; a length outside
  * [1, max_pages*64] sets MLA_ERR_SEQ_LEN and the sequence is skipped.
@@ -196,7 +236,7 @@ mla_status mla_out_proj(const mla_params* p, const void* o_lat, const void* w_uv
  *   flags     : MLA_APPEND_RMSNORM | MLA_APPEND_ROPE (0 stores rows as given)
  * Latent: x / sqrt(mean(x^2)) (gain 1, eps 0), rounded to bf16.
  * k_pe: half-split RoPE (pair i with i+32, angle pos*10000^(-i/32)),
- * computed in fp64, rounded to bf16.  For MLA_KV_E4M3 the bf16 row is then
+ * computed in fp64, rounded to bf16.  For the E4M3 kv_dtypes the bf16 row is then
  * quantised with one fp32 scale per token, scale = max|v| / 448 (1 for a
  * zero row), code = E4M3(v / scale) with fp32 division, round to nearest
  * even, saturating; kv_scale[slot] receives the scale.

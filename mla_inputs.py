@@ -50,7 +50,7 @@ class Workload:
     L: int = 0                   # fixed length for every sequence (0 = ragged)
     ragged: tuple = ()           # (lo, hi) for log-uniform lengths
     pages: str = "contiguous"    # contiguous | permuted | pool
-    kv_dtype: str = "bf16"       # bf16 | e4m3
+    kv_dtype: str = "bf16"       # bf16 | e4m3 | e4m3_mma | e4m3_mma1 (the last three: one cache format)
     out_dtype: str = "f32"       # f32 | bf16
     splits: int = 0              # KV partitions to request (0 = automatic)
     q_len: int = 1               # query tokens per sequence (the newest positions)
@@ -69,6 +69,9 @@ WORKLOADS = {
                        pages="pool"),
     "fp8_batch": Workload("fp8_batch", B=128, H=128, L=8192, seed=4,
                           kv_dtype="e4m3", out_dtype="bf16"),
+    # the same E4M3 cache multiplied as codes on the 8-bit tensor cores
+    "fp8_mma": Workload("fp8_mma", B=128, H=128, L=8192, seed=4,
+                        kv_dtype="e4m3_mma", out_dtype="bf16"),
     # two query tokens per sequence (speculative / multi-token decode)
     "mtp2": Workload("mtp2", B=32, H=128, L=4096, seed=5, q_len=2),
 }

@@ -17,7 +17,9 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmla.so")
 
 MLA_OK, MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED, MLA_ERR_CUDA = 0, 1, 2, 3
 MLA_ERR_PAGE_OOB, MLA_ERR_WORKSPACE, MLA_ERR_SEQ_LEN, MLA_ERR_TIMEOUT = 4, 5, 6, 7
-MLA_KV_BF16, MLA_KV_E4M3 = 0, 1
+MLA_KV_BF16, MLA_KV_E4M3, MLA_KV_E4M3_MMA, MLA_KV_E4M3_MMA1 = 0, 1, 2, 3
+# kv_dtype names: the cache format, and for E4M3 how mla_decode multiplies it
+KV_DTYPES = {"bf16": MLA_KV_BF16, "e4m3": MLA_KV_E4M3, "e4m3_mma": MLA_KV_E4M3_MMA, "e4m3_mma1": MLA_KV_E4M3_MMA1}
 MLA_OUT_F32, MLA_OUT_BF16 = 0, 1
 MLA_APPEND_RMSNORM, MLA_APPEND_ROPE = 1, 2
 
@@ -40,7 +42,7 @@ def make_params(B, H, max_pages_per_seq, num_pages, kv_dtype="bf16", out_dtype="
                 softmax_scale=None) -> MlaParams:
     return MlaParams(B, H, 512, 64, 128, 128, 64, max_pages_per_seq, num_pages,
                      1.0 / math.sqrt(192.0) if softmax_scale is None else softmax_scale,
-                     MLA_KV_E4M3 if kv_dtype == "e4m3" else MLA_KV_BF16,
+                     KV_DTYPES[kv_dtype],
                      MLA_OUT_BF16 if out_dtype == "bf16" else MLA_OUT_F32)
 
 
@@ -51,6 +53,8 @@ _SIGS = {
     "mla_decode_num_splits": (ctypes.c_int, [ctypes.POINTER(MlaParams), ctypes.c_int]),
     "mla_decode_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(MlaParams), ctypes.c_int]),
     "mla_workspace_offsets": (None, [ctypes.POINTER(MlaParams), ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]),
+    "mla_workspace_query_offsets": (None, [ctypes.POINTER(MlaParams), ctypes.c_int,
+                                           ctypes.POINTER(ctypes.c_size_t)]),
     "mla_absorb_q": (ctypes.c_int, [ctypes.POINTER(MlaParams), _P, _P, _P, _P]),
     "mla_decode": (ctypes.c_int, [ctypes.POINTER(MlaParams), _P, _P, _P, _P, _P, _P, _P, ctypes.c_int,
                                   _P, ctypes.c_size_t, _P, _P, _P]),
@@ -117,6 +121,12 @@ def mla_decode_workspace_size(p: MlaParams, num_splits: int = 0) -> int:
 def mla_workspace_offsets(p: MlaParams, num_splits: int = 0):
     arr = (ctypes.c_size_t * 5)()
     lib.mla_workspace_offsets(ctypes.byref(p), num_splits, arr)
+    return list(arr)
+
+
+def mla_workspace_query_offsets(p: MlaParams, num_splits: int = 0):
+    arr = (ctypes.c_size_t * 2)()
+    lib.mla_workspace_query_offsets(ctypes.byref(p), num_splits, arr)
     return list(arr)
 
 

@@ -39,7 +39,9 @@ mla_status check_params(const mla_params* p) {
   if (p->B < 1 || p->H < 1 || p->max_pages_per_seq < 1 || p->num_pages < 1)
     return MLA_ERR_INVALID_ARG;
   if (!(p->softmax_scale > 0.f) || !isfinite(p->softmax_scale)) return MLA_ERR_INVALID_ARG;
-  if (p->kv_dtype != MLA_KV_BF16 && p->kv_dtype != MLA_KV_E4M3) return MLA_ERR_INVALID_ARG;
+  if (p->kv_dtype != MLA_KV_BF16 && p->kv_dtype != MLA_KV_E4M3 && p->kv_dtype != MLA_KV_E4M3_MMA &&
+      p->kv_dtype != MLA_KV_E4M3_MMA1)
+    return MLA_ERR_INVALID_ARG;
   if (p->out_dtype != MLA_OUT_F32 && p->out_dtype != MLA_OUT_BF16) return MLA_ERR_INVALID_ARG;
   if (p->kv_lora_rank != kLatent || p->rope_dim != kRope || p->nope_dim != kNope ||
       p->v_dim != kV || p->page_size != kPage)
@@ -62,6 +64,13 @@ int resolve_splits(const mla_params* p, int num_splits) {
 }
 
 mla_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA; }
+
+// The decode and combine kernels move 16 bytes at a time.
+bool aligned16(const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15) == 0; }
+
+bool is_e4m3(const mla_params* p) { return p->kv_dtype != MLA_KV_BF16; }
+bool is_mma8(const mla_params* p) { return p->kv_dtype == MLA_KV_E4M3_MMA || p->kv_dtype == MLA_KV_E4M3_MMA1; }
+WsLayout layout_of(const mla_params* p, int G) { return ws_layout(p->B, p->H, G, is_mma8(p)); }
 
 }  // namespace
 
@@ -94,7 +103,7 @@ void mla_workspace_offsets(const mla_params* p, int num_splits, size_t offsets[5
     if (offsets) memset(offsets, 0, 5 * sizeof(size_t));
     return;
   }
-  WsLayout l = ws_layout(p->B, p->H, G);
+  WsLayout l = layout_of(p, G);
   offsets[0] = l.err;
   offsets[1] = l.rec;
   offsets[2] = l.seq_start;
@@ -102,10 +111,22 @@ void mla_workspace_offsets(const mla_params* p, int num_splits, size_t offsets[5
   offsets[4] = l.part_o;
 }
 
+void mla_workspace_query_offsets(const mla_params* p, int num_splits, size_t offsets[2]) {
+  if (!offsets) return;
+  const int G = mla_decode_num_splits(p, num_splits);
+  if (G < 1) {
+    offsets[0] = offsets[1] = 0;
+    return;
+  }
+  const WsLayout l = layout_of(p, G);
+  offsets[0] = l.q8;
+  offsets[1] = l.q8_scale;
+}
+
 size_t mla_decode_workspace_size(const mla_params* p, int num_splits) {
   const int G = mla_decode_num_splits(p, num_splits);
   if (G < 1) return 0;
-  return ws_layout(p->B, p->H, G).total;
+  return layout_of(p, G).total;
 }
 
 mla_status mla_absorb_q(const mla_params* p, const void* q_nope, const void* w_uk, void* q_lat,
@@ -128,11 +149,13 @@ mla_status mla_decode(const mla_params* p, const void* q_lat, const void* q_pe,
   if (s != MLA_OK) return s;
   if (!q_lat || !q_pe || !ckv_cache || !kpe_cache || !page_table || !seq_lens || !o_lat)
     return MLA_ERR_INVALID_ARG;
-  const bool fp8 = p->kv_dtype == MLA_KV_E4M3;
-  if (fp8 != (kv_scale != nullptr)) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q_lat) || !aligned16(q_pe) || !aligned16(o_lat) || !aligned16(ckv_cache) || !aligned16(kpe_cache) ||
+      !aligned16(kv_scale) || !aligned16(workspace))
+    return MLA_ERR_INVALID_ARG;
+  if (is_e4m3(p) != (kv_scale != nullptr)) return MLA_ERR_INVALID_ARG;
   const int G = resolve_splits(p, num_splits);
   if (G < 1) return MLA_ERR_INVALID_ARG;
-  const WsLayout l = ws_layout(p->B, p->H, G);
+  const WsLayout l = layout_of(p, G);
   if (!workspace || ws_bytes < l.total) return MLA_ERR_WORKSPACE;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   DecodeArgs a;
@@ -150,12 +173,24 @@ mla_status mla_decode(const mla_params* p, const void* q_lat, const void* q_pe,
   a.seq_start = reinterpret_cast<int*>(ws + l.seq_start);
   a.part_lse = reinterpret_cast<float*>(ws + l.part_lse);
   a.part_o = reinterpret_cast<__nv_bfloat16*>(ws + l.part_o);
+  a.q8 = nullptr;
+  a.q8_scale = nullptr;
+  a.q_terms = a.p_terms = 0;
   a.B = p->B;
   a.H = p->H;
   a.G = G;
   a.maxp = p->max_pages_per_seq;
   a.num_pages = p->num_pages;
   a.scale_log2 = p->softmax_scale * kLog2e;
+  if (is_mma8(p)) {
+    const int terms = p->kv_dtype == MLA_KV_E4M3_MMA ? 2 : 1;
+    a.q8 = ws + l.q8;
+    a.q8_scale = reinterpret_cast<const float*>(ws + l.q8_scale);
+    a.q_terms = a.p_terms = terms;
+    const cudaError_t e = launch_quantize_q(a.q_lat, a.q_pe, (long long)p->B * p->H, terms, ws + l.q8,
+                                            reinterpret_cast<float*>(ws + l.q8_scale), (cudaStream_t)stream);
+    if (e != cudaSuccess) return MLA_ERR_CUDA;
+  }
   return cuda_status(launch_decode_tc(a, (cudaStream_t)stream));
 }
 
@@ -163,10 +198,10 @@ mla_status mla_split_kv_combine(const mla_params* p, const void* workspace, size
                                 int num_splits, void* o_lat, float* lse, mla_stream_t stream) {
   mla_status s = check_params(p);
   if (s != MLA_OK) return s;
-  if (!o_lat) return MLA_ERR_INVALID_ARG;
+  if (!o_lat || !aligned16(o_lat) || !aligned16(workspace)) return MLA_ERR_INVALID_ARG;
   const int G = resolve_splits(p, num_splits);
   if (G < 1) return MLA_ERR_INVALID_ARG;
-  const WsLayout l = ws_layout(p->B, p->H, G);
+  const WsLayout l = layout_of(p, G);
   if (!workspace || ws_bytes < l.total) return MLA_ERR_WORKSPACE;
   const uint8_t* ws = static_cast<const uint8_t*>(workspace);
   return cuda_status(launch_combine(reinterpret_cast<const __nv_bfloat16*>(ws + l.part_o),
@@ -196,7 +231,7 @@ mla_status mla_cache_append(const mla_params* p, const void* kv_rows, const int3
   if (T == 0) return MLA_OK;
   if (!kv_rows || !slots || !ckv_cache || !kpe_cache) return MLA_ERR_INVALID_ARG;
   if ((flags & MLA_APPEND_ROPE) && !positions) return MLA_ERR_INVALID_ARG;
-  const bool fp8 = p->kv_dtype == MLA_KV_E4M3;
+  const bool fp8 = is_e4m3(p);
   if (fp8 && !kv_scale) return MLA_ERR_INVALID_ARG;
   return cuda_status(launch_cache_append(static_cast<const __nv_bfloat16*>(kv_rows), slots,
                                          positions, T, flags, fp8,

@@ -24,12 +24,14 @@ constexpr float kLn2 = 0.6931471805599453f;
 // Workspace layout (see mla_decode_workspace_size in the header).
 // ----------------------------------------------------------------------------
 struct WsLayout {
-  size_t err, rec, seq_start, part_lse, part_o, total;
+  size_t err, rec, seq_start, part_lse, part_o, q8, q8_scale, total;
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-__host__ __device__ inline WsLayout ws_layout(int B, int H, int G) {
+// q8: the 8-bit tensor-core decode also keeps the E4M3 query there (codes
+// [B,H,2,576], scales [B,H] fp32); otherwise those two offsets are 0.
+__host__ __device__ inline WsLayout ws_layout(int B, int H, int G, bool q8 = false) {
   WsLayout l;
   l.err = 0;
   l.rec = 256;
@@ -37,6 +39,12 @@ __host__ __device__ inline WsLayout ws_layout(int B, int H, int G) {
   l.part_lse = align_up(l.seq_start + (size_t)(B + 1) * 4, 256);
   l.part_o = align_up(l.part_lse + (size_t)2 * G * H * 4, 256);
   l.total = align_up(l.part_o + (size_t)2 * G * H * kLatent * 2, 256);
+  l.q8 = l.q8_scale = 0;
+  if (q8) {
+    l.q8 = l.total;
+    l.q8_scale = align_up(l.q8 + (size_t)B * H * 2 * kRow, 256);
+    l.total = align_up(l.q8_scale + (size_t)B * H * 4, 256);
+  }
   return l;
 }
 
@@ -55,6 +63,9 @@ struct DecodeArgs {
   int* seq_start;              // [B+1]
   float* part_lse;             // [2G,H]
   __nv_bfloat16* part_o;       // [2G,H,512], normalised
+  const uint8_t* q8;           // 8-bit tensor-core decode: E4M3 query [B,H,2,576]
+  const float* q8_scale;       // [B,H]
+  int q_terms, p_terms;        // E4M3 terms of the query and of the probabilities (1 or 2)
   int B, H, G, maxp, num_pages;
   float scale_log2;            // softmax_scale * log2(e)
 };

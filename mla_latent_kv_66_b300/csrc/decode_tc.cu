@@ -65,27 +65,45 @@ constexpr uint32_t kXBytes = 4 * kSlab;
 // [64 x 128 B] boxes, its 32 rope codes ([64 x 32 B]) and the page's 64 fp32
 // scales; after expansion the bf16 stage also carries the scales.
 constexpr uint32_t kRawKpe = 2 * 8192, kRawScale = kRawKpe + 2048, kRawBytes = kRawScale + 256;
-constexpr uint32_t kStageScale = kStageBf;
-constexpr int kMaxStages = 4;
+// E4M3 cache on the 8-bit tensor cores: a stage holds the codes as the MMAs
+// read them, two [64 x 128 B] latent boxes (128-byte swizzle), the
+// [64 x 32 B] RoPE box (32-byte swizzle) and the page's 64 scales.
+constexpr uint32_t kStage8Kpe = 2 * 8192, kStage8Scale = kStage8Kpe + 2048, kStage8Bytes = 19 * 1024;
+static_assert(kStage8Kpe == kRawKpe && kStage8Scale == kRawScale, "one copy schedule for both E4M3 layouts");
+constexpr int kMaxStages = 7;
 
-template <bool kFp8>
+// kMode: 0 bf16 cache; 1 E4M3 cache expanded exactly to bf16; 2 E4M3 cache on
+// the 8-bit tensor cores (E4M3 query and probabilities).
+template <int kMode>
 struct Layout {
-  static constexpr int kStages = kFp8 ? 3 : 4;   // bf16 stages the MMAs read
-  static constexpr int kRaw = kFp8 ? 2 : 0;      // raw E4M3 pages
-  static constexpr uint32_t kStageBytes = kFp8 ? kStageBf + 1024 : kStageBf;
+  static constexpr bool kExp = kMode == 1, kMma8 = kMode == 2;
+  static constexpr int kStages = kMma8 ? 7 : kExp ? 3 : 4;   // stages the MMAs read
+  static constexpr int kRaw = kExp ? 2 : 0;                  // raw E4M3 pages (expanded path)
+  static constexpr uint32_t kStageBytes = kMma8 ? kStage8Bytes : kExp ? kStageBf + 1024 : kStageBf;
+  static constexpr uint32_t kStageScale = kMma8 ? kStage8Scale : kStageBf;  // token scales in a stage
   static constexpr uint32_t kOffRaw = kStages * kStageBytes;
-  static constexpr uint32_t kOffQpe = kOffRaw + kRaw * kRawBytes;  // [128 x 32] bf16, 64-byte swizzle
+  // query RoPE part (A operand of the RoPE MMAs): bf16 [128 x 32], 64-byte
+  // swizzle; 8-bit: two E4M3 terms of [128 x 32 B], 32-byte swizzle, 4 KB apart
+  static constexpr uint32_t kOffQpe = kOffRaw + kRaw * kRawBytes;
   static constexpr uint32_t kOffX = kOffQpe + 8192;                // the peer's partial score tile
   static constexpr uint32_t kOffXs = kOffX + kXBytes;              // own partial, outgoing
   static constexpr uint32_t kSmemBytes = kOffXs + kXBytes + 1024;
+  static constexpr uint32_t kStaticSmem = kMma8 ? 7 * 1024 : 4 * 1024;  // static shared memory, rounded up
   static_assert(kStageBytes % 1024 == 0 && kRawBytes % 128 == 0 && kOffQpe % 512 == 0,
-                "swizzled tiles need 1024-byte (128 B swizzle) / 512-byte (64 B) alignment");
+                "swizzled tiles need 1024-byte (128 B swizzle) / 512-byte (64 B, 32 B) alignment");
   static_assert(kStages <= kMaxStages, "stage barriers");
-  static_assert(kSmemBytes + 4096 <= 232448, "shared memory per CTA (with the static part, < 4 KB)");
+  static_assert(kSmemBytes + kStaticSmem <= 232448, "shared memory per CTA");
 };
 constexpr uint32_t kTmO = 0, kTmS = 256, kTmP = 320, kTmQ = 384;
+// 8-bit mode: P buffer pb holds term t of its 64 probabilities (4 codes per
+// column) at kTmP + 32 pb + 16 t; the query's latent codes, term t, at
+// kTmQ + 64 t.
 constexpr int kThreads = 512;
 constexpr float kRescaleLog2 = 8.f;  // lazy rescale threshold: P stays <= 2^8
+// 8-bit mode: P = 2^(x - m + kPShift8) with the lazy threshold kRescaleLog2_8,
+// so P <= 2^8 < 448 (the largest E4M3 value) and E4M3's normal range covers
+// the 14 octaves below the running maximum.
+constexpr float kRescaleLog2_8 = 2.f, kPShift8 = 6.f;
 constexpr int kIdRing = 16;          // page ids read ahead by the producer
 
 enum {
@@ -240,6 +258,12 @@ __device__ inline uint32_t e4m3x2_to_bf16x2(uint32_t v) {
   const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
   return pack_bf16(f.x, f.y);
 }
+// Two fp32 values as an E4M3 pair (nearest even, saturating): lo in the low byte.
+__device__ inline uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
 __device__ inline float ld_shared_f32(uint32_t addr) {
   float v;
   asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
@@ -295,16 +319,54 @@ __device__ inline void load_q_rows(const DecodeArgs& a, uint32_t tq, uint32_t qp
   }
 }
 
-template <bool kFp8>
+// Row h of this CTA's half of sequence b's E4M3 query, every term t <
+// a.q_terms: its 256 latent codes into 64 tensor-memory columns at tq + 64 t
+// (four codes per column) and its 32 RoPE codes into shared memory at
+// qpe + 4096 t (32-byte swizzle: 16-byte chunk c of row h at
+// h * 32 + ((c ^ ((h >> 2) & 1)) * 16), the A operand of the RoPE MMAs).
+// Rows h >= H are zero.  Returns the row's scale.  The caller waits for the
+// tensor-memory stores and publishes them.
+__device__ inline float load_q8_rows(const DecodeArgs& a, uint32_t tq, uint32_t qpe, int b, int h, uint32_t rank) {
+  const bool on = h < a.H;
+  const uint8_t* row = a.q8 + ((size_t)b * a.H + (on ? h : 0)) * (2 * kRow);
+  for (int t = 0; t < a.q_terms; ++t) {
+    const uint4* src = reinterpret_cast<const uint4*>(row + t * kRow + rank * 256);
+    const uint4* sp = reinterpret_cast<const uint4*>(row + t * kRow + kLatent + rank * 32);
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const uint4 xp = on ? sp[c] : make_uint4(0, 0, 0, 0);
+      st_shared_v4(qpe + t * 4096 + h * 32 + ((c ^ ((h >> 2) & 1)) << 4), xp.x, xp.y, xp.z, xp.w);
+    }
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+      uint32_t r[32];
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        const uint4 x = on ? src[cc * 8 + v] : make_uint4(0, 0, 0, 0);
+        r[4 * v] = x.x;
+        r[4 * v + 1] = x.y;
+        r[4 * v + 2] = x.z;
+        r[4 * v + 3] = x.w;
+      }
+      tc::tmem_st32(tq + t * 64 + cc * 32, r);
+    }
+  }
+  return on ? a.q8_scale[(size_t)b * a.H + h] : 0.f;
+}
+
+template <int kMode>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_ckv,
                      const __grid_constant__ CUtensorMap tm_kpe, DecodeArgs a) {
-  using L = Layout<kFp8>;
+  using L = Layout<kMode>;
+  constexpr bool kFp8 = kMode == 1;  // E4M3 cache expanded to bf16 in shared memory
+  constexpr bool kF8 = kMode == 2;   // E4M3 cache on the 8-bit tensor cores
   constexpr int kStages = L::kStages;
-  constexpr uint32_t kStageBytes = L::kStageBytes;
+  constexpr uint32_t kStageBytes = L::kStageBytes, kStageScale = L::kStageScale;
   constexpr uint32_t kOffQpe = L::kOffQpe, kOffX = L::kOffX, kOffXs = L::kOffXs;
-  // bf16: pages go straight into the stage ring.  E4M3: pages go into the
-  // raw ring (codes and scales) and the exchange warps expand them.
+  // bf16 and 8-bit: pages go straight into the stage ring.  Expanded E4M3:
+  // pages go into the raw ring (codes and scales) and the exchange warps
+  // expand them.
   constexpr int kRing = kFp8 ? L::kRaw : kStages;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bars[B_COUNT];
@@ -316,6 +378,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   __shared__ uint32_t lsum_swap[2 * 128];  // row sums between them at the end of a unit
   __shared__ int page_ids[kIdRing];        // producer-private
   __shared__ int sl_cache[32];             // lengths of the range's first sequences
+  // 8-bit mode: log2 of the current page's token scales (one copy per
+  // exchange warp) and their reciprocals for the softmax (by page parity and
+  // row quarter; 0 past the sequence end)
+  __shared__ __align__(16) float tok_lg[kF8 ? 4 * 64 : 1];  // read as float4
+  __shared__ __align__(16) float tok_inv[kF8 ? 2 * 4 * 64 : 1];
 
   const uint32_t rank = cluster_rank(), peer = rank ^ 1u;
   const int w = blockIdx.x >> 1;
@@ -382,14 +449,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t s = g % kRing;
     int page = page_at(g);
     if (page < 0) page = 0;  // a bad page id: masked by the softmax warps
-    if (kFp8) {
-      const uint32_t fb = bar(B_RFULL + s);
-      const uint32_t raw = base + L::kOffRaw + s * kRawBytes;
+    if (kFp8 || kF8) {
+      // E4M3: this CTA's 256 latent codes (two 128-byte boxes), 32 RoPE codes
+      // and the page's 64 scales; straight into a stage (8-bit) or the raw ring
+      const uint32_t fb = bar(kF8 ? B_FULL + s : B_RFULL + s);
+      const uint32_t dst = kF8 ? base + s * kStageBytes : base + L::kOffRaw + s * kRawBytes;
       mbar_expect_tx(fb, 2 * 8192 + 2048 + kPage * 4);
-      tma_load_2d(raw, &tm_ckv, fb, (int)rank * 256, page * kPage);
-      tma_load_2d(raw + 8192, &tm_ckv, fb, (int)rank * 256 + 128, page * kPage);
-      tma_load_2d(raw + kRawKpe, &tm_kpe, fb, (int)rank * 32, page * kPage);
-      bulk_copy_g2s(raw + kRawScale, a.kv_scale + (size_t)page * kPage, kPage * 4, fb);
+      tma_load_2d(dst, &tm_ckv, fb, (int)rank * 256, page * kPage);
+      tma_load_2d(dst + 8192, &tm_ckv, fb, (int)rank * 256 + 128, page * kPage);
+      tma_load_2d(dst + kRawKpe, &tm_kpe, fb, (int)rank * 32, page * kPage);
+      bulk_copy_g2s(dst + kRawScale, a.kv_scale + (size_t)page * kPage, kPage * 4, fb);
     } else {
       const uint32_t fb = bar(B_FULL + s);
       const uint32_t st = base + s * kStageBytes;
@@ -493,6 +562,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t g = 0, uc = 0;
       bool ok = true;
       const uint32_t idesc_qk = idesc_bf16(128, 64, false, false);
+      const uint32_t idesc_qk8 = idesc_e4m3(128, 64, false, false);
       while (ok && wk.next(a, u)) {
         const int np = u.pe - u.pb;
         if (!mbar_wait(bar(B_QFULL), uc & 1, &abort_flag, a.err)) break;
@@ -510,11 +580,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           // one descriptor per operand and page; K-step kk is a constant offset
           // (16-byte units) into it, so the MMAs issue back to back
           const uint64_t kdesc = sdesc_sw128(st, 16, 1024);
+          if constexpr (kF8) {
+            // 32 codes per K step: 8 steps over the two latent boxes per query
+            // term, then one step per term for the 32 RoPE codes
+            for (int t = 0; t < a.q_terms; ++t) {
 #pragma unroll
-          for (int kk = 0; kk < 16; ++kk)
-            mma_bf16_ts(d, tmem + kTmQ + kk * 8, kdesc + (uint64_t)(((kk >> 2) * kBox + (kk & 3) * 32) >> 4),
-                        idesc_qk, kk > 0 ? 1u : 0u);
-          {  // this CTA's 32 dimensions of the RoPE key: A = q_pe half (shared memory)
+              for (int kk = 0; kk < 8; ++kk)
+                mma_e4m3_ts(d, tmem + kTmQ + t * 64 + kk * 8,
+                            kdesc + (uint64_t)(((kk >> 2) * kBox + (kk & 3) * 32) >> 4), idesc_qk8,
+                            (t > 0 || kk > 0) ? 1u : 0u);
+            }
+            const uint64_t rdesc = sdesc_sw32(st + kStage8Kpe, 16, 256);
+            for (int t = 0; t < a.q_terms; ++t)
+              mma_e4m3_ss(d, sdesc_sw32(base + kOffQpe + t * 4096, 16, 256), rdesc, idesc_qk8, 1u);
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk)
+              mma_bf16_ts(d, tmem + kTmQ + kk * 8, kdesc + (uint64_t)(((kk >> 2) * kBox + (kk & 3) * 32) >> 4),
+                          idesc_qk, kk > 0 ? 1u : 0u);
+            // this CTA's 32 dimensions of the RoPE key: A = q_pe half (shared memory)
             const uint64_t qdesc = sdesc_sw64(base + kOffQpe, 16, 512);
             const uint64_t rdesc = sdesc_sw64(st + 4 * kBox, 16, 512);
 #pragma unroll
@@ -557,6 +641,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t g = 0, uc = 0;
       bool ok = true;
       const uint32_t idesc_pv = idesc_bf16(128, 256, false, true);
+      const uint32_t idesc_pv8 = idesc_e4m3(128, 256, false, true);
       while (ok && wk.next(a, u)) {
         const int np = u.pe - u.pb;
         for (int i = 0; i < np; ++i) {
@@ -567,12 +652,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          // A = P from tensor memory (two bf16 per column), B = the stage's latent
+          // A = P from tensor memory, B = the stage's latent (MN-major)
           const uint64_t cdesc = sdesc_sw128(base + s * kStageBytes, kBox, 1024);
+          if constexpr (kF8) {
+            // four codes per column, 32 tokens (4096 bytes of codes) per K step
+            for (int t = 0; t < a.p_terms; ++t) {
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_bf16_ts(tmem + kTmO, tmem + kTmP + pb * 32 + kk * 8, cdesc + kk * 128, idesc_pv,
-                        (i > 0 || kk > 0) ? 1u : 0u);
+              for (int kk = 0; kk < 2; ++kk)
+                mma_e4m3_ts(tmem + kTmO, tmem + kTmP + pb * 32 + t * 16 + kk * 8, cdesc + kk * 256, idesc_pv8,
+                            (i > 0 || t > 0 || kk > 0) ? 1u : 0u);
+            }
+          } else {
+            // two bf16 per column, 16 tokens per K step
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_bf16_ts(tmem + kTmO, tmem + kTmP + pb * 32 + kk * 8, cdesc + kk * 128, idesc_pv,
+                          (i > 0 || kk > 0) ? 1u : 0u);
+          }
           mma_commit(bar(B_PVD + pb));
           mma_commit(bar(B_EMPTY + s));
           if (i == np - 1) mma_commit(bar(B_ODONE));
@@ -603,8 +699,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     // this CTA's half of a later unit's query: 256 latent values -> tensor
     // memory, 32 RoPE values -> shared memory
+    float qs_cur = 0.f, qs_nxt = 0.f;  // 8-bit mode: query row scale of this / the next unit
     auto load_q = [&](const Unit& q) {
-      load_q_rows(a, tmem + lane_base + kTmQ, base + kOffQpe, q.b, h, rank, 0, 2, true);
+      if constexpr (kF8)
+        qs_nxt = load_q8_rows(a, tmem + lane_base + kTmQ, base + kOffQpe, q.b, h, rank);
+      else
+        load_q_rows(a, tmem + lane_base + kTmQ, base + kOffQpe, q.b, h, rank, 0, 2, true);
       tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
@@ -677,7 +777,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint32_t g = 0;
     bool ok = true;
     bool have = wk.next(a, u);
-    if (have) {  // the first unit's query is loaded by the softmax warps
+    if (have) {  // the first unit's query is loaded by the softmax warps (8-bit mode: here)
+      if constexpr (kF8) {
+        load_q(u);
+        qs_cur = qs_nxt;
+      }
       Walker pk = wk;
       Unit nu;
       if (pk.next(a, nu)) prefetch_q(nu.b);
@@ -691,23 +795,47 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int jp = u.pb; jp < u.pe; ++jp, ++g) {
         if (!wwait(B_SFULL, g & 1)) { ok = false; break; }
         tc_fence_after();
+        const float* tsc = reinterpret_cast<const float*>(smem_base + (g % kStages) * kStageBytes + kStageScale);
+        float* lg = tok_lg + q4 * 64;
+        if constexpr (kF8) {
+          // the score of token t is q_scale * scale_t times the score of the
+          // codes; rank 0 also adds log2(scale_t), which carries the token
+          // scale into the probabilities (P . V multiplies codes)
+          lg[lane] = rank == 0 ? __log2f(tsc[lane]) : 0.f;
+          lg[lane + 32] = rank == 0 ? __log2f(tsc[lane + 32]) : 0.f;
+          __syncwarp();
+        }
         float v[64];
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           uint32_t s32[32];
           tmem_ld32(tmem + lane_base + kTmS + half * 32, s32);
           tmem_wait_ld();
+          if constexpr (kF8) {
+            const float cq = c * qs_cur;
+            const float4* t4 = reinterpret_cast<const float4*>(tsc) + half * 8;
+            const float4* l4 = reinterpret_cast<const float4*>(lg) + half * 8;
 #pragma unroll
-          for (int k = 0; k < 32; ++k) v[half * 32 + k] = __uint_as_float(s32[k]) * c;
+            for (int c4 = 0; c4 < 8; ++c4) {
+              const float4 f = t4[c4], o = l4[c4];
+              const int k = half * 32 + 4 * c4;
+              v[k] = fmaf(__uint_as_float(s32[4 * c4]), cq * f.x, o.x);
+              v[k + 1] = fmaf(__uint_as_float(s32[4 * c4 + 1]), cq * f.y, o.y);
+              v[k + 2] = fmaf(__uint_as_float(s32[4 * c4 + 2]), cq * f.z, o.z);
+              v[k + 3] = fmaf(__uint_as_float(s32[4 * c4 + 3]), cq * f.w, o.w);
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) v[half * 32 + k] = __uint_as_float(s32[k]) * c;
+          }
         }
         tc_fence_before();
         mbar_arrive(bar(B_SFREE));
         if constexpr (kFp8) {
           // E4M3: the score of token t is scale_t times the score of its codes
           // (scales copied next to the expanded stage)
-          const float* sca = reinterpret_cast<const float*>(smem_base + (g % kStages) * kStageBytes + kStageScale);
 #pragma unroll
-          for (int k = 0; k < 64; ++k) v[k] *= sca[k];
+          for (int k = 0; k < 64; ++k) v[k] *= tsc[k];
         }
         if (g >= 1) {
           // our receive slab of this quarter is free once our softmax warps have
@@ -720,6 +848,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           // our outgoing slab (and the peer's receive slab) is free once the
           // peer's softmax warps have read page g-1
           if (!wwait_c(B_XFREE + q4, (g - 1) & 1)) { ok = false; break; }
+        }
+        if constexpr (kF8) {
+          // 1 / scale_t for this quarter's softmax warps (0 past the sequence
+          // end); they finished page g-2, which used this slot, before
+          // reading page g-1 (waited for above)
+          float* inv = tok_inv + ((g & 1) * 4 + q4) * 64;
+          const int nv = min(kPage, u.n - jp * kPage);
+          inv[lane] = lane < nv ? __frcp_rn(tsc[lane]) : 0.f;
+          inv[lane + 32] = lane + 32 < nv ? __frcp_rn(tsc[lane + 32]) : 0.f;
         }
         uint8_t* xt = smem_base + kOffXs;
 #pragma unroll
@@ -735,6 +872,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         // the next unit's query goes in once this unit's last S = Q K^T is done
         if (jp == u.pe - 1 && have_next) load_q(nu);
+        if (jp == u.pe - 1) qs_cur = qs_nxt;
         // the next page's expansion waits for the P . V that frees its stage,
         // so it comes after this page's exchange
         if (kFp8 && g + 1 < npages && !expand(g + 1)) { ok = false; break; }
@@ -756,6 +894,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
     const int H = a.H;
     uint32_t xk = 0;  // phases of the warpgroup-exchange barrier consumed
+    constexpr float kShift = kF8 ? kPShift8 : 0.f;  // P = 2^(x - m + kShift)
 
     // Swap one value per row with the other warpgroup's warp of the same row
     // quarter (bounded wait).  Row maxima alternate between two slots, so that
@@ -783,7 +922,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint32_t g = 0, uc = 0;
     bool ok = true;
     bool have = wk.next(a, u);
-    if (have) {  // the first unit's query: warpgroup j loads half j of the latent part
+    if (have && !kF8) {  // the first unit's query: warpgroup j loads half j of the latent part
       load_q_rows(a, tmem + lane_base + kTmQ, base + kOffQpe, u.b, h, rank, j, j + 1, j == 0);
       tmem_wait_st();
       fence_proxy_async_smem();
@@ -853,14 +992,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // and take the same decisions
         float alpha = 1.f;
         bool resc = false;
-        if (mx > m + kRescaleLog2) {
+        if (mx > m + (kF8 ? kRescaleLog2_8 : kRescaleLog2)) {
           alpha = ex2(m - mx);
           resc = i > 0;
           m = mx;
         }
-        const float mm = m == -INFINITY ? 0.f : m;
+        const float mm = (m == -INFINITY ? 0.f : m) - kShift;
         float ps[4] = {0.f, 0.f, 0.f, 0.f};
         uint32_t pk[16];
+        if constexpr (kF8) {
+          // x carries log2(scale_t) (added by rank 0), so P = 2^(x - mm) is
+          // the probability times the token scale, as P . V on the codes needs
+          // it; the row sum takes P / scale_t.  P becomes two E4M3 terms:
+          // Veltkamp's split (fp32, explicit roundings) gives hi with 4
+          // significant bits, exact in E4M3's normal range, and lo = P - hi
+          // exactly; each pair of terms is one conversion.
+          const float* inv = tok_inv + ((gi & 1) * 4 + q4) * 64 + 32 * j;
+#pragma unroll
+          for (int kq = 0; kq < 8; ++kq) {
+            float hi[4], lo[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int k = 4 * kq + e;
+              const float pe = ex2(x[k] - mm);
+              ps[e] = fmaf(pe, inv[k], ps[e]);  // inv is 0 past the sequence end
+              const float c = __fmul_rn(pe, 1048577.f);  // (2^20 + 1) P
+              hi[e] = __fsub_rn(c, __fsub_rn(c, pe));
+              lo[e] = __fsub_rn(pe, hi[e]);
+            }
+            pk[kq] = f32x2_to_e4m3x2(hi[0], hi[1]) | (f32x2_to_e4m3x2(hi[2], hi[3]) << 16);
+            pk[8 + kq] = f32x2_to_e4m3x2(lo[0], lo[1]) | (f32x2_to_e4m3x2(lo[2], lo[3]) << 16);
+          }
+          // a bad page: every P is 0, but the scales read in its place may be
+          // anything (0 * inf)
+          if (!page_ok) ps[0] = ps[1] = ps[2] = ps[3] = 0.f;
+        } else {
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
           const float p0 = ex2(x[2 * k] - mm), p1 = ex2(x[2 * k + 1] - mm);
@@ -876,13 +1042,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             pk[k] = pack_bf16(p0, p1);
           }
         }
+        }
         l = l * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
 
         // zero cache rows past the sequence end (garbage could be NaN)
         if (valid < kPage) {
           const uint32_t st = base + s * kStageBytes;
           const int rows = kPage - valid, per_box = rows * 8;
-          for (int idx = h + 128 * j; idx < 4 * per_box; idx += 256) {
+          constexpr int kBoxes = kF8 ? 2 : 4;  // latent boxes of a stage (128-byte rows)
+          for (int idx = h + 128 * j; idx < kBoxes * per_box; idx += 256) {
             const int box = idx / per_box, rem = idx % per_box;
             st_shared_v4(st + box * kBox + (valid + rem / 8) * 128 + (rem % 8) * 16, 0, 0, 0, 0);
           }
@@ -909,8 +1077,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           tmem_wait_st();
         }
-        // this warpgroup's 32 tokens of P: 16 tensor-memory columns of bf16 pairs
-        tmem_st16(tmem + lane_base + kTmP + pb * 32 + j * 16, pk);
+        if constexpr (kF8) {
+          // this warpgroup's 32 tokens of P, each term in 8 columns of four codes
+          uint32_t hi8[8], lo8[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            hi8[k] = pk[k];
+            lo8[k] = pk[8 + k];
+          }
+          tmem_st8(tmem + lane_base + kTmP + pb * 32 + j * 8, hi8);
+          if (a.p_terms == 2) tmem_st8(tmem + lane_base + kTmP + pb * 32 + 16 + j * 8, lo8);
+        } else {
+          // this warpgroup's 32 tokens of P: 16 tensor-memory columns of bf16 pairs
+          tmem_st16(tmem + lane_base + kTmP + pb * 32 + j * 16, pk);
+        }
         tmem_wait_st();
         fence_proxy_async_smem();  // the zeroed stage rows above
         tc_fence_before();
@@ -950,7 +1130,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
       if (rank == 0 && j == 0 && h < H) {
-        const float lse = lt > 0.f ? (m + log2f(lt)) * kLn2 : -INFINITY;
+        const float lse = lt > 0.f ? (m - kShift + log2f(lt)) * kLn2 : -INFINITY;
         if (!u.split) {
           if (a.lse) a.lse[row] = lse;
         } else {
@@ -981,8 +1161,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 // Clusters of the decode kernel that fit on the device at once (0 on error).
 int decode_tc_max_clusters() {
-  constexpr uint32_t smem = Layout<false>::kSmemBytes;
-  if (cudaFuncSetAttribute(decode_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  constexpr uint32_t smem = Layout<0>::kSmemBytes;
+  if (cudaFuncSetAttribute(decode_tc_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem) != cudaSuccess)
     return 0;
   cudaLaunchConfig_t cfg = {};
@@ -990,17 +1170,21 @@ int decode_tc_max_clusters() {
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, decode_tc_kernel<false>, &cfg) != cudaSuccess) return 0;
+  if (cudaOccupancyMaxActiveClusters(&n, decode_tc_kernel<0>, &cfg) != cudaSuccess) return 0;
   return n;
 }
 
 // bf16 cache: tiles TMA-loaded straight into the 128-byte-swizzled stages.
 // E4M3 cache (kv_scale != null): raw tiles without swizzle, expanded in the
-// kernel.
+// kernel; or, with the E4M3 query (q8 != null), tiles in the layouts the
+// 8-bit MMAs read (128-byte swizzle for the latent, 32-byte for k_pe).
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t stream) {
-  const bool fp8 = a.kv_scale != nullptr;
+  const bool fp8 = a.kv_scale != nullptr, mma8 = fp8 && a.q8 != nullptr;
   if ((reinterpret_cast<uintptr_t>(a.ckv) & 15) || (reinterpret_cast<uintptr_t>(a.kpe) & 15) ||
       (reinterpret_cast<uintptr_t>(a.kv_scale) & 15))
+    return cudaErrorInvalidValue;
+  if (mma8 && (a.q_terms < 1 || a.q_terms > 2 || a.p_terms < 1 || a.p_terms > 2 || !a.q8_scale ||
+               (reinterpret_cast<uintptr_t>(a.q8) & 15)))
     return cudaErrorInvalidValue;
   CUtensorMap tc_map, tk_map;
   const cuuint64_t rows = (cuuint64_t)a.num_pages * kPage;
@@ -1009,8 +1193,10 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t stream) {
   const cuuint64_t kd[2] = {kRope, rows}, ks[1] = {kRope * es};
   if (fp8) {
     const cuuint32_t cbox[2] = {128, 64}, kbox[2] = {32, 64};
-    if (!make_tmap(&tc_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.ckv, cd, cs, cbox, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !make_tmap(&tk_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.kpe, kd, ks, kbox, CU_TENSOR_MAP_SWIZZLE_NONE))
+    if (!make_tmap(&tc_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.ckv, cd, cs, cbox,
+                   mma8 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_tmap(&tk_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.kpe, kd, ks, kbox,
+                   mma8 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_NONE))
       return cudaErrorInvalidValue;
   } else {
     const cuuint32_t box[2] = {64, 64}, kbox[2] = {32, 64};
@@ -1019,8 +1205,8 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t stream) {
                    CU_TENSOR_MAP_SWIZZLE_64B))
       return cudaErrorInvalidValue;
   }
-  auto kernel = fp8 ? decode_tc_kernel<true> : decode_tc_kernel<false>;
-  const uint32_t smem = fp8 ? Layout<true>::kSmemBytes : Layout<false>::kSmemBytes;
+  auto kernel = mma8 ? decode_tc_kernel<2> : fp8 ? decode_tc_kernel<1> : decode_tc_kernel<0>;
+  const uint32_t smem = mma8 ? Layout<2>::kSmemBytes : fp8 ? Layout<1>::kSmemBytes : Layout<0>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   return launch_dependent(kernel, dim3(2 * a.G), dim3(kThreads), smem, stream, tc_map, tk_map, a);

@@ -17,6 +17,8 @@ cudaError_t launch_cache_append(const __nv_bfloat16* rows, const int32_t* slots,
                                 void* kpe, float* scale, cudaStream_t stream);
 cudaError_t launch_multi_token_expand(const int32_t* page_table, const int32_t* seq_lens, int B, int T, int maxp,
                                       int32_t* table_out, int32_t* lens_out, cudaStream_t stream);
+cudaError_t launch_quantize_q(const __nv_bfloat16* q_lat, const __nv_bfloat16* q_pe, long long rows, int terms,
+                              uint8_t* codes, float* scale, cudaStream_t stream);
 cudaError_t launch_rope_q(const __nv_bfloat16* q_raw, const int32_t* seq_lens, __nv_bfloat16* q,
                           int B, int H, cudaStream_t stream);
 

@@ -51,6 +51,21 @@ def test_workspace_layout_matches_the_documented_formula():
     assert L.mla_decode_workspace_size(p, G) == total
 
 
+def test_workspace_query_region_of_the_8bit_decode():
+    G, up = 5, (lambda x: (x + 255) // 256 * 256)
+    base = L.mla_decode_workspace_size(L.make_params(7, 128, 10, 70, "e4m3"), G)
+    for kv in ("e4m3_mma", "e4m3_mma1"):
+        p = L.make_params(B=7, H=128, max_pages_per_seq=10, num_pages=70, kv_dtype=kv)
+        codes = base
+        scale = up(codes + 7 * 128 * 2 * 576)
+        assert L.mla_workspace_query_offsets(p, G) == [codes, scale]
+        assert L.mla_decode_workspace_size(p, G) == up(scale + 7 * 128 * 4)
+        # the rest of the layout is the one of the other kv_dtypes
+        assert L.mla_workspace_offsets(p, G) == L.mla_workspace_offsets(L.make_params(7, 128, 10, 70), G)
+    for kv in ("bf16", "e4m3"):
+        assert L.mla_workspace_query_offsets(L.make_params(7, 128, 10, 70, kv), G) == [0, 0]
+
+
 def _call_decode(p, ws_bytes=1 << 30, G=4, scale=None, nulls=()):
     fake = ctypes.c_void_p(0x1000)
     args = [fake] * 7
@@ -66,8 +81,22 @@ def test_host_argument_checks_return_before_any_launch():
     assert _call_decode(p, nulls=(0,)) == L.MLA_ERR_INVALID_ARG
     assert _call_decode(p, ws_bytes=16) == L.MLA_ERR_WORKSPACE
     assert _call_decode(p, G=-1) == L.MLA_ERR_INVALID_ARG
-    # bf16 cache with a scale pointer is a contradiction
+    # bf16 cache with a scale pointer is a contradiction, an E4M3 cache without one too
     assert _call_decode(p, scale=ctypes.c_void_p(0x2000)) == L.MLA_ERR_INVALID_ARG
+    for kv in ("e4m3", "e4m3_mma", "e4m3_mma1"):
+        assert _call_decode(L.make_params(B=2, H=128, max_pages_per_seq=4, num_pages=8, kv_dtype=kv)) == \
+            L.MLA_ERR_INVALID_ARG
+    bad = L.make_params(B=2, H=128, max_pages_per_seq=4, num_pages=8)
+    bad.kv_dtype = 4
+    assert _call_decode(bad) == L.MLA_ERR_INVALID_ARG
+    # the kernels move 16 bytes at a time: an unaligned tensor is refused
+    fake, odd = ctypes.c_void_p(0x1000), ctypes.c_void_p(0x1008)
+    for i in range(3):
+        args = [fake] * 3
+        args[i] = odd
+        assert L.lib.mla_decode(ctypes.byref(p), args[0], args[1], fake, fake, None, fake, fake, 4, args[2],
+                                1 << 30, fake, None, None) == L.MLA_ERR_INVALID_ARG
+    assert L.lib.mla_split_kv_combine(ctypes.byref(p), fake, 1 << 30, 4, odd, None, None) == L.MLA_ERR_INVALID_ARG
     bad = L.make_params(B=2, H=128, max_pages_per_seq=4, num_pages=8)
     bad.kv_lora_rank = 256
     assert _call_decode(bad) == L.MLA_ERR_UNSUPPORTED
