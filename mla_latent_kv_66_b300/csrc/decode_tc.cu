@@ -95,9 +95,9 @@ struct Layout {
   static_assert(kSmemBytes + kStaticSmem <= 232448, "shared memory per CTA");
 };
 constexpr uint32_t kTmO = 0, kTmS = 256, kTmP = 320, kTmQ = 384;
-// 8-bit mode: P buffer pb holds term t of its 64 probabilities (4 codes per
-// column) at kTmP + 32 pb + 16 t; the query's latent codes, term t, at
-// kTmQ + 64 t.
+// 8-bit mode: P buffer pb holds term t of tokens [32 j, 32 j + 32) (4 codes
+// per column) at kTmP + 32 pb + 16 j + 8 t; the query's latent codes, term t,
+// at kTmQ + 64 t.
 constexpr int kThreads = 512;
 constexpr float kRescaleLog2 = 8.f;  // lazy rescale threshold: P stays <= 2^8
 // 8-bit mode: P = 2^(x - m + kPShift8) with the lazy threshold kRescaleLog2_8,
@@ -655,11 +655,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           // A = P from tensor memory, B = the stage's latent (MN-major)
           const uint64_t cdesc = sdesc_sw128(base + s * kStageBytes, kBox, 1024);
           if constexpr (kF8) {
-            // four codes per column, 32 tokens (4096 bytes of codes) per K step
+            // four codes per column, 32 tokens (4096 bytes of codes) per K
+            // step; tokens [32 kk, 32 kk + 32) of term t at 16 kk + 8 t
             for (int t = 0; t < a.p_terms; ++t) {
 #pragma unroll
               for (int kk = 0; kk < 2; ++kk)
-                mma_e4m3_ts(tmem + kTmO, tmem + kTmP + pb * 32 + t * 16 + kk * 8, cdesc + kk * 256, idesc_pv8,
+                mma_e4m3_ts(tmem + kTmO, tmem + kTmP + pb * 32 + kk * 16 + t * 8, cdesc + kk * 256, idesc_pv8,
                             (i > 0 || t > 0 || kk > 0) ? 1u : 0u);
             }
           } else {
@@ -831,6 +832,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         tc_fence_before();
         mbar_arrive(bar(B_SFREE));
+        float inv_a = 0.f, inv_b = 0.f;
+        if constexpr (kF8) {
+          const int nv = min(kPage, u.n - jp * kPage);
+          inv_a = lane < nv ? __frcp_rn(tsc[lane]) : 0.f;
+          inv_b = lane + 32 < nv ? __frcp_rn(tsc[lane + 32]) : 0.f;
+        }
         if constexpr (kFp8) {
           // E4M3: the score of token t is scale_t times the score of its codes
           // (scales copied next to the expanded stage)
@@ -854,9 +861,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           // end); they finished page g-2, which used this slot, before
           // reading page g-1 (waited for above)
           float* inv = tok_inv + ((g & 1) * 4 + q4) * 64;
-          const int nv = min(kPage, u.n - jp * kPage);
-          inv[lane] = lane < nv ? __frcp_rn(tsc[lane]) : 0.f;
-          inv[lane + 32] = lane + 32 < nv ? __frcp_rn(tsc[lane + 32]) : 0.f;
+          inv[lane] = inv_a;
+          inv[lane + 32] = inv_b;
         }
         uint8_t* xt = smem_base + kOffXs;
 #pragma unroll
@@ -1003,10 +1009,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if constexpr (kF8) {
           // x carries log2(scale_t) (added by rank 0), so P = 2^(x - mm) is
           // the probability times the token scale, as P . V on the codes needs
-          // it; the row sum takes P / scale_t.  P becomes two E4M3 terms:
-          // Veltkamp's split (fp32, explicit roundings) gives hi with 4
-          // significant bits, exact in E4M3's normal range, and lo = P - hi
-          // exactly; each pair of terms is one conversion.
+          // it; the row sum takes P / scale_t.  P becomes E4M3 terms: hi is P
+          // rounded to 4 significant bits (half up; exact in E4M3's normal
+          // range, P >= 0), lo = P - hi exactly (|lo| <= 2^-4 P), rounded to
+          // E4M3; each pair of codes is one conversion (the lo codes go
+          // unused with one term).
           const float* inv = tok_inv + ((gi & 1) * 4 + q4) * 64 + 32 * j;
 #pragma unroll
           for (int kq = 0; kq < 8; ++kq) {
@@ -1015,10 +1022,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             for (int e = 0; e < 4; ++e) {
               const int k = 4 * kq + e;
               const float pe = ex2(x[k] - mm);
-              ps[e] = fmaf(pe, inv[k], ps[e]);  // inv is 0 past the sequence end
-              const float c = __fmul_rn(pe, 1048577.f);  // (2^20 + 1) P
-              hi[e] = __fsub_rn(c, __fsub_rn(c, pe));
+              hi[e] = __uint_as_float((__float_as_uint(pe) + 0x80000u) & 0xFFF00000u);
               lo[e] = __fsub_rn(pe, hi[e]);
+              ps[e] = fmaf(pe, inv[k], ps[e]);  // inv is 0 past the sequence end
             }
             pk[kq] = f32x2_to_e4m3x2(hi[0], hi[1]) | (f32x2_to_e4m3x2(hi[2], hi[3]) << 16);
             pk[8 + kq] = f32x2_to_e4m3x2(lo[0], lo[1]) | (f32x2_to_e4m3x2(lo[2], lo[3]) << 16);
@@ -1077,20 +1083,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           tmem_wait_st();
         }
-        if constexpr (kF8) {
-          // this warpgroup's 32 tokens of P, each term in 8 columns of four codes
-          uint32_t hi8[8], lo8[8];
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            hi8[k] = pk[k];
-            lo8[k] = pk[8 + k];
-          }
-          tmem_st8(tmem + lane_base + kTmP + pb * 32 + j * 8, hi8);
-          if (a.p_terms == 2) tmem_st8(tmem + lane_base + kTmP + pb * 32 + 16 + j * 8, lo8);
-        } else {
-          // this warpgroup's 32 tokens of P: 16 tensor-memory columns of bf16 pairs
-          tmem_st16(tmem + lane_base + kTmP + pb * 32 + j * 16, pk);
-        }
+        // this warpgroup's 32 tokens of P in 16 tensor-memory columns: bf16
+        // pairs, or (8-bit) the hi term's codes in 8 columns, then the lo term's
+        tmem_st16(tmem + lane_base + kTmP + pb * 32 + j * 16, pk);
         tmem_wait_st();
         fence_proxy_async_smem();  // the zeroed stage rows above
         tc_fence_before();
