@@ -28,6 +28,7 @@ sys.path.insert(0, ROOT)
 
 import mla_inputs as mi  # noqa: E402
 
+E2E_STEPS = 8  # steps recorded in one graph by the end-to-end leg
 METRIC = "MLA decode tokens/s and latent-cache HBM GB/s (% of ~8 TB/s roofline), 1 B300"
 FLUSH_BYTES = 256 << 20
 
@@ -244,10 +245,9 @@ def run_ours(args, w, rank, world):
                      G, step.workspace, step.o_lat, step.lse)
         if ev:
             ev[1].record()
-        L.mla_split_kv_combine(p, step.workspace, G, step.o_lat, step.lse)
-        L.mla_out_proj(p, step.o_lat, st["w_uv"], step.out)
+        L.mla_combine_out_proj(p, step.workspace, G, step.o_lat, st["w_uv"], step.out, step.lse)
 
-    # the step as a CUDA graph (the four launches recorded once)
+    # the step as a CUDA graph (its launches recorded once)
     step.capture(*args_step)
     for _ in range(max(3, args.warmup)):
         flush.zero_()
@@ -296,11 +296,13 @@ def run_ours(args, w, rank, world):
     # end to end: every step's per-token inputs (q_nope, rotated q_pe, page
     # table, lengths) packed in one pinned host buffer and copied in with one
     # host-to-device copy, the step, and its output copied back to pinned host
-    # memory.  Steps are pipelined over two buffer sets (two steps, each
-    # recorded as a graph): copies run on their own stream while the other
-    # set's step computes; a set is reused only after its previous output has
-    # been copied out.  No L2 flush inside the pipeline: the cache (151 MB for
-    # v2_layer) is larger than the L2.
+    # memory.  Steps alternate between two buffer sets so that one set's
+    # copies overlap the other's compute (a set's inputs are rewritten only
+    # after its previous step has read them, its output buffer only after it
+    # has been copied out); E2E_STEPS such steps are recorded as one CUDA graph
+    # (copies on their own streams), so the host issues one launch per
+    # E2E_STEPS steps.  No L2 flush inside: the cache (151 MB for v2_layer) is
+    # larger than the L2.
     inp = st["inp"]
     names = ("q_nope", "q_pe", "table", "lens")
     offs, total = {}, 0
@@ -320,45 +322,56 @@ def run_ours(args, w, rank, world):
         for nm in names:
             view(host_pack, nm).copy_(st[nm].cpu())
         devb = {nm: view(dev_pack, nm) for nm in names}
-        stp = step if k == 0 else mla.MLADecodeStep(w.B, w.H, table_np.shape[1], inp["num_pages"], w.kv_dtype,
-                                                     w.out_dtype, w.splits, dev, q_len=w.q_len)
-        dev_pack.copy_(host_pack)  # the capture runs the step once: give it real inputs
-        stp.capture(devb["q_nope"], devb["q_pe"], st["w_uk"], st["w_uv"], st["ckv"], st["kpe"], st["sc"],
-                    devb["table"], devb["lens"])
+        stp = mla.MLADecodeStep(w.B, w.H, table_np.shape[1], inp["num_pages"], w.kv_dtype, w.out_dtype, w.splits,
+                                dev, q_len=w.q_len)
+        sargs = (devb["q_nope"], devb["q_pe"], st["w_uk"], st["w_uv"], st["ckv"], st["kpe"], st["sc"], devb["table"],
+                 devb["lens"])
+        dev_pack.copy_(host_pack)
+        stp(*sargs)  # first-call set-up outside the capture
         out_h = torch.empty(stp.out.shape, dtype=stp.out.dtype).pin_memory()
-        sets.append(dict(host=host_pack, dev=dev_pack, step=stp, out_h=out_h))
+        sets.append(dict(host=host_pack, dev=dev_pack, step=stp, args=sargs, out_h=out_h))
+    torch.cuda.synchronize()
     h2d = sum(st[k].numel() * st[k].element_size() for k in names)
     d2h = sets[0]["out_h"].numel() * sets[0]["out_h"].element_size()
-    s_comp, s_in, s_out = torch.cuda.current_stream(), torch.cuda.Stream(), torch.cuda.Stream()
-    n_e2e = max(3, args.warmup) + min(K, 500)
-    ev_h2d = [torch.cuda.Event() for _ in range(n_e2e)]
-    ev_done = [torch.cuda.Event() for _ in range(n_e2e)]
-    ev_d2h = [torch.cuda.Event() for _ in range(n_e2e)]
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    n_warm = max(3, args.warmup)
-    for i in range(n_e2e):
-        k = sets[i % 2]
-        if i == n_warm:
-            t_start.record(s_in)
-        with torch.cuda.stream(s_in):  # inputs in
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        cap = torch.cuda.current_stream()
+        ev_done, ev_d2h = [], []
+        for i in range(E2E_STEPS):
+            k = sets[i % 2]
             if i >= 2:
                 s_in.wait_event(ev_done[i - 2])  # the set's previous step has read its inputs
-            k["dev"].copy_(k["host"], non_blocking=True)
-            ev_h2d[i].record(s_in)
-        s_comp.wait_event(ev_h2d[i])
-        if i >= 2:
-            s_comp.wait_event(ev_d2h[i - 2])  # the set's previous output has been copied out
-        k["step"].replay()
-        ev_done[i].record(s_comp)
-        with torch.cuda.stream(s_out):  # output out
-            s_out.wait_event(ev_done[i])
-            k["out_h"].copy_(k["step"].out, non_blocking=True)
-            ev_d2h[i].record(s_out)
-    t_end.record(s_out)
+            else:
+                s_in.wait_stream(cap)
+            with torch.cuda.stream(s_in):
+                k["dev"].copy_(k["host"], non_blocking=True)
+            e_in = torch.cuda.Event()
+            e_in.record(s_in)
+            cap.wait_event(e_in)
+            if i >= 2:
+                cap.wait_event(ev_d2h[i - 2])  # the set's previous output has been copied out
+            k["step"](*k["args"])
+            ev_done.append(torch.cuda.Event())
+            ev_done[-1].record(cap)
+            s_out.wait_event(ev_done[-1])
+            with torch.cuda.stream(s_out):
+                k["out_h"].copy_(k["step"].out, non_blocking=True)
+            ev_d2h.append(torch.cuda.Event())
+            ev_d2h[-1].record(s_out)
+        cap.wait_stream(s_in)
+        cap.wait_stream(s_out)
+    reps = max(1, min(K, 500) // E2E_STEPS)
+    for _ in range(max(3, args.warmup) // E2E_STEPS + 1):
+        graph.replay()
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
-    e2e_ms = [t_start.elapsed_time(t_end) / (n_e2e - n_warm)]
-    e2e, = max_over_ranks([statistics.mean(e2e_ms)], world, dev)
+    t_start.record()
+    for _ in range(reps):
+        graph.replay()
+    t_end.record()
+    torch.cuda.synchronize()
+    e2e, = max_over_ranks([t_start.elapsed_time(t_end) / (reps * E2E_STEPS)], world, dev)
     status = step.status()
     return dict(ms=ms, dec_ms=dms, e2e_ms=e2e, h2d=h2d, d2h=d2h, wall=wall, clocks=clk.summary(),
                 status=status, G=G, tokens=int(inp["seq_lens"].sum()))
@@ -468,8 +481,9 @@ def main():
     cfg = {"workload": w.name, "B": w.B, "H": w.H, "L": w.L or "log-uniform[%d,%d]" % w.ragged, "q_len": w.q_len,
            "kv_lora_rank": 512, "rope_dim": 64, "page_size": 64, "kv_dtype": w.kv_dtype,
            "pages": w.pages, "l2": "flushed before every timed step (256 MiB write)",
-           "step": "CUDA graph: q absorption, decode, split-KV combine, out-projection",
-           "e2e": "pinned host inputs and output copied every step, steps pipelined over two buffer sets, "
+           "step": "CUDA graph: q absorption, decode, split-KV combine fused into the out-projection",
+           "e2e": "pinned host inputs and output copied every step; steps alternate two buffer sets (copies "
+                  "overlap the other set's compute), %d steps per CUDA graph; " % E2E_STEPS +
                   "no L2 flush (cache larger than the L2)",
            "parallelism": "replicas" if world > 1 else "single-gpu"}
     if args.impl == "reference":
@@ -536,7 +550,9 @@ def main():
         "cpu_baseline": cpu,
         "e2e": {"value": job_tokens_per_s(world, tokens_per_step, r["e2e_ms"]), "unit": "tokens/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
-        "gpu_launches": 4 * args.steps,
+        # per step: absorption, (E4M3 tensor-core path: query quantisation),
+        # decode, combine + out-projection; several query tokens: the row expansion
+        "gpu_launches": (3 + (w.kv_dtype in ("e4m3_mma", "e4m3_mma1")) + (w.q_len > 1)) * args.steps,
         "clocks": r["clocks"], "status": r["status"], "num_splits": r["G"], "wall_s_timed": r["wall"],
     }
     print(json.dumps(out), flush=True)

@@ -226,6 +226,25 @@ mla_status mla_out_proj(const mla_params* p, const void* o_lat, const void* w_uv
                         void* out, mla_stream_t stream);
 
 /* ---------------------------------------------------------------------
+ * mla_combine_out_proj: mla_split_kv_combine and mla_out_proj in one launch
+ * (decompression and attention as one layer, page section
+ * "源码里的压缩全流程").  For every (b, h) the kernel for head h builds
+ * o_lat[b,h] in shared memory -- read from o_lat where mla_decode finished
+ * the sequence, merged from the workspace's partials where it was split --
+ * and multiplies it by W_UV[h] there, so a merged latent is not read back
+ * from memory before its product.  Results equal mla_split_kv_combine
+ * followed by mla_out_proj whenever mla_split_kv_combine takes its grouped
+ * form (B * ceil(H/8) >= 2 x the SM count), and agree to rounding otherwise.
+ * Must follow mla_decode on the same stream with the same params,
+ * num_splits and workspace.
+ *   o_lat : [B,H,512] bf16, read (finished sequences) and written (split
+ *           sequences);  lse : [B,H] fp32 or NULL, written for split sequences
+ *   w_uv, out : as mla_out_proj
+ */
+mla_status mla_combine_out_proj(const mla_params* p, const void* workspace, size_t ws_bytes, int num_splits,
+                                void* o_lat, float* lse, const void* w_uv, void* out, mla_stream_t stream);
+
+/* ---------------------------------------------------------------------
  * mla_cache_append: write T new tokens into the paged cache (the step before
  * decode, page section "源码里的压缩全流程": the down-projection row is split into the
  * 512-d latent and the 64-d k_pe, the latent is RMS-normalised, RoPE is

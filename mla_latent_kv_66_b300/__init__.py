@@ -10,7 +10,7 @@ _BINDINGS = ("MLAError", "MlaParams", "make_params", "mla_absorb_q", "mla_cache_
              "mla_decode_num_splits", "mla_decode_workspace_size", "mla_out_proj", "mla_rope_q",
              "mla_split_kv_combine", "mla_workspace_offsets", "mla_workspace_status", "status_string",
              "mla_multi_token_expand", "mla_decode_static", "mla_decode_static_status",
-             "mla_workspace_query_offsets", "KV_DTYPES",
+             "mla_workspace_query_offsets", "KV_DTYPES", "mla_combine_out_proj",
              "MLA_APPEND_RMSNORM", "MLA_APPEND_ROPE", "LIB_PATH")
 
 

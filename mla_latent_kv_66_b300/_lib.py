@@ -61,6 +61,8 @@ _SIGS = {
     "mla_split_kv_combine": (ctypes.c_int, [ctypes.POINTER(MlaParams), _P, ctypes.c_size_t, ctypes.c_int,
                                             _P, _P, _P]),
     "mla_out_proj": (ctypes.c_int, [ctypes.POINTER(MlaParams), _P, _P, _P, _P]),
+    "mla_combine_out_proj": (ctypes.c_int, [ctypes.POINTER(MlaParams), _P, ctypes.c_size_t, ctypes.c_int, _P, _P,
+                                            _P, _P, _P]),
     "mla_cache_append": (ctypes.c_int, [ctypes.POINTER(MlaParams), _P, _P, _P, ctypes.c_int, ctypes.c_int,
                                         _P, _P, _P, _P]),
     "mla_rope_q": (ctypes.c_int, [ctypes.POINTER(MlaParams), _P, _P, _P, _P]),
@@ -152,6 +154,13 @@ def mla_split_kv_combine(p, workspace, num_splits, o_lat, lse=None, stream=None)
 def mla_out_proj(p, o_lat, w_uv, out, stream=None):
     _check(lib.mla_out_proj(ctypes.byref(p), _ptr(o_lat), _ptr(w_uv), _ptr(out), _stream(stream)),
            "mla_out_proj")
+
+
+def mla_combine_out_proj(p, workspace, num_splits, o_lat, w_uv, out, lse=None, stream=None):
+    _check(lib.mla_combine_out_proj(ctypes.byref(p), _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(), num_splits,
+                                    _ptr(o_lat), _ptr(lse), _ptr(w_uv), _ptr(out), _stream(stream)),
+           "mla_combine_out_proj")
 
 
 def mla_cache_append(p, kv_rows, slots, positions, flags, ckv, kpe, kv_scale=None, stream=None):

@@ -8,6 +8,7 @@
 // normalised over its own range.
 #include <atomic>
 
+#include "combine.cuh"
 #include "kernels.h"
 #include "tc.cuh"
 #include "tmap.cuh"
@@ -113,12 +114,8 @@ __global__ void __launch_bounds__(128) combine_head_kernel(const __nv_bfloat16* 
   if (t == 0 && lse_out) lse_out[(size_t)b * H + h] = mx + logf(sum);
 }
 
-// Grouped form: one CTA per (sequence, group of kHeads heads) of a split sequence; warp j
-// merges head kHeads * blockIdx.y + j and lane l owns latent columns
-// [16l, 16l+16).  The partials of the sequence are the records of the
-// workers whose page ranges it overlaps, in page order; a warp takes them 32
-// at a time (one per lane for the slot and log-sum-exp), keeping a running
-// maximum so that each partial is read once.
+// Grouped form: one CTA per (sequence, group of kHeads heads) of a split
+// sequence; warp j merges head kHeads * blockIdx.y + j (warp_merge_partials).
 constexpr int kHeads = 8;
 
 __global__ void __launch_bounds__(32 * kHeads) combine_group_kernel(const __nv_bfloat16* __restrict__ part_o,
@@ -126,99 +123,23 @@ __global__ void __launch_bounds__(32 * kHeads) combine_group_kernel(const __nv_b
                                                               const int* __restrict__ seq_start,
                                                               __nv_bfloat16* __restrict__ o_lat,
                                                               float* __restrict__ lse_out, int B, int H, int G) {
-  __shared__ int s_wf, s_n;
-  __shared__ long long s_sb, s_P;
+  __shared__ SeqWorkers s_sw;
   grid_dep_wait();  // the decode kernel's partials
   grid_dep_trigger();
   const int b = blockIdx.x, t = threadIdx.x, lane = t & 31;
   const int h = blockIdx.y * kHeads + (t >> 5);
-  if (t == 0) {  // the workers holding this sequence's pages (one thread: 64-bit divisions)
-    const long long P = seq_start[B];
-    const long long sb = seq_start[b], se = seq_start[b + 1];
-    int wf = 0, n = 0;
-    if (se > sb) {
-      wf = worker_of(sb, G, P);
-      n = worker_of(se - 1, G, P) - wf + 1;
-    }
-    s_wf = wf;
-    s_n = n;
-    s_sb = sb;
-    s_P = P;
-  }
+  if (t == 0) s_sw = seq_workers(seq_start, B, G, b);
   __syncthreads();
-  const int wf = s_wf, n = s_n;
-  const long long sb = s_sb, P = s_P;
-  if (n <= 1 || h >= H) return;  // empty, or finished by the decode kernel
-  // slot of partial i, or -1 for an empty worker range (no partial written)
-  auto slot_of = [&](int i) {
-    const int w = wf + i;
-    const long long lo = range_lo(w, G, P), hi = range_lo(w + 1, G, P);
-    return lo == hi ? -1 : (sb <= lo ? w : G + w);
-  };
-  float m = -INFINITY, sum = 0.f, acc[16];
-#pragma unroll
-  for (int k = 0; k < 16; ++k) acc[k] = 0.f;
-  for (int c0 = 0; c0 < n; c0 += 32) {
-    const int i = c0 + lane;
-    const int sl = i < n ? slot_of(i) : -1;
-    const float l = sl >= 0 ? part_lse[(size_t)sl * H + h] : -INFINITY;
-    float cm = l;
-#pragma unroll
-    for (int o = 16; o; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
-    const float nm = fmaxf(m, cm);
-    if (nm > m && m != -INFINITY) {  // rescale what the earlier chunks added
-      const float r = __expf(m - nm);
-      sum *= r;
-#pragma unroll
-      for (int k = 0; k < 16; ++k) acc[k] *= r;
-    }
-    m = nm;
-    const float wt = l == -INFINITY ? 0.f : __expf(l - m);
-    float ws = wt;
-#pragma unroll
-    for (int o = 16; o; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
-    sum += ws;
-    const int cn = min(32, n - c0);
-    for (int k0 = 0; k0 < cn; k0 += 4) {
-      uint4 v[4][2];
-      float wk[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {  // four partials' loads in flight
-        const int k = k0 + u;
-        const int slk = __shfl_sync(0xffffffffu, sl, k & 31);
-        wk[u] = __shfl_sync(0xffffffffu, wt, k & 31);
-        if (k < cn && slk >= 0) {
-          const uint4* src = reinterpret_cast<const uint4*>(part_o + ((size_t)slk * H + h) * kLatent) + 2 * lane;
-          v[u][0] = src[0];
-          v[u][1] = src[1];
-        } else {
-          v[u][0] = v[u][1] = make_uint4(0, 0, 0, 0);
-          wk[u] = 0.f;
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const uint32_t w8[8] = {v[u][0].x, v[u][0].y, v[u][0].z, v[u][0].w,
-                                v[u][1].x, v[u][1].y, v[u][1].z, v[u][1].w};
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          acc[2 * e] = fmaf(wk[u], bf16lo(w8[e]), acc[2 * e]);
-          acc[2 * e + 1] = fmaf(wk[u], bf16hi(w8[e]), acc[2 * e + 1]);
-        }
-      }
-    }
-  }
-  const float inv = sum > 0.f ? 1.f / sum : 0.f;
+  const SeqWorkers sw = s_sw;
+  if (sw.n <= 1 || h >= H) return;  // empty, or finished by the decode kernel
+  float acc[16];
+  const float lse = warp_merge_partials(part_o, part_lse, sw, G, H, h, acc);
   uint32_t o8[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    __nv_bfloat162 q = __floats2bfloat162_rn(acc[2 * e] * inv, acc[2 * e + 1] * inv);
-    o8[e] = *reinterpret_cast<uint32_t*>(&q);
-  }
+  pack_row16(acc, o8);
   uint4* dst = reinterpret_cast<uint4*>(o_lat + ((size_t)b * H + h) * kLatent) + 2 * lane;
   dst[0] = make_uint4(o8[0], o8[1], o8[2], o8[3]);
   dst[1] = make_uint4(o8[4], o8[5], o8[6], o8[7]);
-  if (lane == 0 && lse_out) lse_out[(size_t)b * H + h] = sum > 0.f ? m + logf(sum) : -INFINITY;
+  if (lane == 0 && lse_out) lse_out[(size_t)b * H + h] = lse;
 }
 
 // SM count of the current device, cached per device (it only picks the

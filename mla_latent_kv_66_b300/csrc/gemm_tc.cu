@@ -12,6 +12,7 @@
 // latent axis as M, i.e. as an MN-major A operand; W_UV is K-major.
 #include <algorithm>
 
+#include "combine.cuh"
 #include "kernels.h"
 #include "tc.cuh"
 #include "tmap.cuh"
@@ -154,6 +155,175 @@ __global__ void __launch_bounds__(128, 1)
   }
 }
 
+// ---------------------------------------------------------------- combine + out-projection
+// The split-KV combine fused into the out-projection: CTA (head h, batch
+// tile) builds its B operand, o_lat[b, h, :] for the tile's sequences, in
+// shared memory -- read from o_lat for a sequence the decode finished, merged
+// from the partials (warp_merge_partials, the grouped combine's arithmetic)
+// for a split one, which is also written to o_lat / lse -- while W_UV[h]
+// streams in by TMA; then the same MMAs as the out-projection.  The merged
+// latent never leaves the SM before its product.
+struct FusedArgs {
+  int B, H, N, S, G;
+  const __nv_bfloat16* weight;  // W_UV, prefetched into L2 before the dependency wait
+  const __nv_bfloat16* part_o;
+  const float* part_lse;
+  const int* seq_start;
+  __nv_bfloat16* o_lat;
+  float* lse;
+  void* out;
+  int out_bf16;
+};
+
+constexpr int kFusedThreads = 512;  // 16 warps: two B-operand rows per warp at N = 32
+constexpr int kFusedMaxN = 128;
+
+__global__ void __launch_bounds__(kFusedThreads, 1)
+    outproj_combine_kernel(const __grid_constant__ CUtensorMap tA, FusedArgs g) {
+  constexpr int KB = 8;  // K blocks of 64 latent columns
+  const int S = g.S;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bars[2 * kMaxS + 1];
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+  __shared__ SeqWorkers s_sw[kFusedMaxN];  // the decode workers of each row's sequence
+
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t bblk = (uint32_t)g.N * 128u;                 // one K block of the B operand
+  const uint32_t bbase = base + (uint32_t)S * kABytes;         // B operand: KB blocks of [N x 128 B]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.x, nt = blockIdx.z;
+  const uint32_t full = smem_u32(&bars[0]), empty = smem_u32(&bars[kMaxS]), done = smem_u32(&bars[2 * kMaxS]);
+  const uint32_t ncols = g.N <= 32 ? 32 : g.N <= 64 ? 64 : 128;
+
+  if (threadIdx.x == 32) prefetch_l2(g.weight + (size_t)h * kV * kLatent, kV * kLatent * 2);
+  grid_dep_wait();  // the decode's o_lat and partials
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int i = 0; i < S; ++i) {
+      mbar_init(full + 8 * i, 1);
+      mbar_init(empty + 8 * i, 1);
+    }
+    mbar_init(done, 1);
+    fence_mbar_init();
+    prefetch_tmap(&tA);
+  }
+  if (warp == 2) {
+    tmem_alloc(smem_u32(&tmem_slot), ncols);
+    tmem_relinquish();
+  }
+  if (threadIdx.x >= 64 && threadIdx.x - 64 < g.N && nt * g.N + (int)threadIdx.x - 64 < g.B)
+    s_sw[threadIdx.x - 64] = seq_workers(g.seq_start, g.B, g.G, nt * g.N + (int)threadIdx.x - 64);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  // the weight's first S K blocks in flight before the combine work
+  int issued = 0;  // (producer thread)
+  auto issue = [&](int kb) {
+    const int s = kb % S;
+    const uint32_t a_s = base + s * kABytes;
+    mbar_expect_tx(full + 8 * s, kABytes);
+    tma_load_2d(a_s, &tA, full + 8 * s, kb * 64, h * 128);
+    ++issued;
+  };
+  if (warp == 0 && lane == 0)
+    for (int kb = 0; kb < S && kb < KB; ++kb) issue(kb);
+
+  // B operand rows: warp w takes rows w, w + 8, ...; lane l holds latent
+  // columns [16 l, 16 l + 16), i.e. 16-byte chunks 2(l%4), 2(l%4)+1 of K block l/4
+  for (int r = warp; r < g.N; r += kFusedThreads / 32) {
+    const int b = nt * g.N + r;
+    uint32_t o8[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    if (b < g.B) {
+      const SeqWorkers sw = s_sw[r];
+      uint4* row = reinterpret_cast<uint4*>(g.o_lat + ((size_t)b * g.H + h) * kLatent) + 2 * lane;
+      if (sw.n <= 1) {  // finished by the decode (or empty)
+        const uint4 v0 = row[0], v1 = row[1];
+        o8[0] = v0.x; o8[1] = v0.y; o8[2] = v0.z; o8[3] = v0.w;
+        o8[4] = v1.x; o8[5] = v1.y; o8[6] = v1.z; o8[7] = v1.w;
+      } else {
+        float acc[16];
+        const float l = warp_merge_partials(g.part_o, g.part_lse, sw, g.G, g.H, h, acc);
+        pack_row16(acc, o8);
+        row[0] = make_uint4(o8[0], o8[1], o8[2], o8[3]);
+        row[1] = make_uint4(o8[4], o8[5], o8[6], o8[7]);
+        if (lane == 0 && g.lse) g.lse[(size_t)b * g.H + h] = l;
+      }
+    }
+    const uint32_t blk = bbase + (uint32_t)(lane >> 2) * bblk + (uint32_t)r * 128u;
+    const uint32_t c0 = 2u * (lane & 3);
+    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(blk + ((c0 ^ (r & 7)) << 4)), "r"(o8[0]), "r"(o8[1]),
+                 "r"(o8[2]), "r"(o8[3])
+                 : "memory");
+    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(blk + (((c0 + 1) ^ (r & 7)) << 4)), "r"(o8[4]),
+                 "r"(o8[5]), "r"(o8[6]), "r"(o8[7])
+                 : "memory");
+  }
+  fence_proxy_async_smem();  // the B operand, for the tensor cores
+  __syncthreads();
+
+  if (warp == 0 && lane == 0) {
+    // the rest of the weight's K blocks
+    for (int kb = S; kb < KB; ++kb) {
+      const int s = kb % S;
+      if (!mbar_wait(empty + 8 * s, ((kb / S) - 1) & 1, &abort_flag, nullptr)) break;
+      issue(kb);
+    }
+  } else if (warp == 1 && lane == 0) {
+    const uint32_t idesc = idesc_bf16(128, g.N, false, false);
+    for (int kb = 0; kb < KB; ++kb) {
+      const int s = kb % S;
+      if (!mbar_wait(full + 8 * s, (kb / S) & 1, &abort_flag, nullptr)) break;
+      tc_fence_after();
+      const uint32_t a_s = base + s * kABytes, b_s = bbase + kb * bblk;
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        mma_bf16_ss(tmem, sdesc_sw128(a_s + k * 32, 16, 1024), sdesc_sw128(b_s + k * 32, 16, 1024), idesc,
+                    (kb | k) != 0 ? 1u : 0u);
+      mma_commit(empty + 8 * s);
+    }
+    mma_commit(done);
+  }
+  __syncwarp();
+
+  // epilogue (warps 0-3, one per 32 tensor-memory lanes): thread = v row, columns = batch
+  const bool ok = mbar_wait(done, 0, &abort_flag, nullptr) && !abort_flag;
+  tc_fence_after();
+  if (warp < 4) {
+    const int row = warp * 32 + lane;
+    for (int c0 = 0; c0 < g.N; c0 += 16) {
+      uint32_t r[16];
+      tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, r);
+      tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int b = nt * g.N + c0 + j;
+        if (b >= g.B) break;
+        const float v = ok ? __uint_as_float(r[j]) : __int_as_float(0x7fc00000);
+        const size_t bh = (size_t)b * g.H + h;
+        if (g.out_bf16)
+          static_cast<__nv_bfloat16*>(g.out)[bh * kV + row] = __float2bfloat16_rn(v);
+        else
+          static_cast<float*>(g.out)[bh * kV + row] = v;
+      }
+    }
+  }
+  if (abort_flag && warp == 0 && lane == 0) {  // copies in flight land before the CTA exits
+    for (int kb = issued - 1; kb >= 0 && kb >= issued - S; --kb) {
+      volatile int no_abort = 0;
+      mbar_wait(full + 8 * (kb % S), (kb / S) & 1, &no_abort, nullptr);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, ncols);
+  }
+}
+
 int batch_tile(int B) {
   const int n = (B + 15) / 16 * 16;
   return n < 256 ? n : 256;
@@ -208,6 +378,26 @@ cudaError_t launch_out_proj_tc(const __nv_bfloat16* o_lat, const __nv_bfloat16* 
   if (e != cudaSuccess) return e;
   dim3 grid(H, 1, (B + N - 1) / N);
   return launch_dependent(gemm_tc_kernel<1>, grid, dim3(128), smem, stream, tA, tB, g);
+}
+
+cudaError_t launch_outproj_combine(const __nv_bfloat16* part_o, const float* part_lse, const int* seq_start,
+                                   __nv_bfloat16* o_lat, float* lse, const __nv_bfloat16* w_uv, void* out,
+                                   bool out_bf16, int B, int H, int G, cudaStream_t stream) {
+  if (!aligned16(o_lat) || !aligned16(w_uv) || !aligned16(part_o)) return cudaErrorInvalidValue;
+  const int N = std::min(batch_tile(B), kFusedMaxN);
+  CUtensorMap tA;
+  const cuuint64_t ad[2] = {kLatent, (cuuint64_t)H * kV}, as[1] = {kLatent * 2};
+  const cuuint32_t abox[2] = {64, 128};
+  if (!make_tmap(&tA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w_uv, ad, as, abox)) return cudaErrorInvalidValue;
+  // the B operand (N KB) stays; as many weight K blocks in flight as fit
+  const size_t bbytes = (size_t)N * 128 * 8;
+  const int S = (int)std::min<size_t>(kMaxS, ((200u << 10) - bbytes) / kABytes);
+  FusedArgs g{B, H, N, S, G, w_uv, part_o, part_lse, seq_start, o_lat, lse, out, out_bf16 ? 1 : 0};
+  const size_t smem = S * kABytes + bbytes + 1024;
+  cudaError_t e = cudaFuncSetAttribute(outproj_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(H, 1, (B + N - 1) / N);
+  return launch_dependent(outproj_combine_kernel, grid, dim3(kFusedThreads), smem, stream, tA, g);
 }
 
 }  // namespace mla

@@ -1,8 +1,9 @@
 """One MLA decode step over a resident paged latent cache, through the C ABI:
-absorb the query (W_UK), latent attention with split-KV, combine, and the
-value out-projection (W_UV).  Buffers are allocated once, at construction;
-a step over fixed input buffers can be recorded once as a CUDA graph and
-replayed, which removes the host launch overhead of the four calls."""
+absorb the query (W_UK), latent attention with split-KV, then the combine
+and the value out-projection (W_UV), fused into one launch by default.
+Buffers are allocated once, at construction; a step over fixed input buffers
+can be recorded once as a CUDA graph and replayed, which removes the host
+launch overhead of the calls."""
 from __future__ import annotations
 
 import torch
@@ -15,12 +16,15 @@ class MLADecodeStep:
     positions, causal); queries are [B,q_len,H,...] and the output
     [B,q_len,H,128].  The page table and lengths passed to a call are the B
     sequences'; the step expands them into B*q_len rows (expand_rows), whose
-    lengths are also what mla_rope_q needs to rotate the queries."""
+    lengths are also what mla_rope_q needs to rotate the queries.
+    fused=False runs mla_split_kv_combine and mla_out_proj as two launches
+    instead of mla_combine_out_proj."""
 
     def __init__(self, B, H, max_pages_per_seq, num_pages, kv_dtype="bf16", out_dtype="f32",
-                 num_splits=0, device="cuda", q_len=1):
+                 num_splits=0, device="cuda", q_len=1, fused=True):
         rows = B * q_len
         self.q_len = q_len
+        self.fused = fused
         self.p_seq = L.make_params(B, H, max_pages_per_seq, num_pages, kv_dtype, out_dtype)
         self.p = L.make_params(rows, H, max_pages_per_seq, num_pages, kv_dtype, out_dtype)
         self.num_splits = L.mla_decode_num_splits(self.p, num_splits)
@@ -52,8 +56,11 @@ class MLADecodeStep:
         L.mla_absorb_q(p, q_nope, w_uk, self.q_lat, stream)
         L.mla_decode(p, self.q_lat, q_pe, ckv, kpe, kv_scale, page_table, seq_lens, G,
                      self.workspace, self.o_lat, self.lse, stream)
-        L.mla_split_kv_combine(p, self.workspace, G, self.o_lat, self.lse, stream)
-        L.mla_out_proj(p, self.o_lat, w_uv, self.out, stream)
+        if self.fused:
+            L.mla_combine_out_proj(p, self.workspace, G, self.o_lat, w_uv, self.out, self.lse, stream)
+        else:
+            L.mla_split_kv_combine(p, self.workspace, G, self.o_lat, self.lse, stream)
+            L.mla_out_proj(p, self.o_lat, w_uv, self.out, stream)
         if self.q_len > 1:
             return self.out.view(-1, self.q_len, *self.out.shape[1:])
         return self.out

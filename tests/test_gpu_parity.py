@@ -279,6 +279,52 @@ def test_host_rejects_bad_arguments_with_an_error():
         L.mla_out_proj(p, x, x, None)
 
 
+# ------------------------------------------------------------------ combine fused into the out-projection
+@pytest.mark.parametrize("lens,G,H", [([700, 64, 1, 130, 65, 2000], 7, 16), ([4096] * 32, 0, 128),
+                                      ([1500] * 40, 64, 128)])
+def test_combine_fused_into_out_projection(lens, G, H):
+    """mla_combine_out_proj against mla_split_kv_combine + mla_out_proj on the
+    same decode: bit-exact (out, o_lat, lse) where the separate combine takes
+    its grouped form (B * ceil(H/8) >= 2 x SMs), within rounding otherwise;
+    and against the oracle."""
+    inp = small_inputs(lens, H=H, seed=29)
+    cache = O.build_cache(inp, garbage=garbage(inp))
+    qpe = O.rope_q_bf16(inp["q_pe_raw"], inp["seq_lens"])
+    B = len(lens)
+    table = inp["page_table"]
+    p = L.make_params(B, H, table.shape[1], inp["num_pages"])
+    G = L.mla_decode_num_splits(p, G)
+    ws = torch.zeros(L.mla_decode_workspace_size(p, G), dtype=torch.uint8, device="cuda")
+    ckv, kpe, sc = upload_cache(cache)
+    q_lat = torch.empty(B, H, 512, dtype=torch.bfloat16, device="cuda")
+    L.mla_absorb_q(p, bf16_dev(inp["q_nope"]), bf16_dev(inp["w_uk"]), q_lat)
+    o_a = torch.full((B, H, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse_a = torch.full((B, H), float("nan"), dtype=torch.float32, device="cuda")
+    L.mla_decode(p, q_lat, bf16_dev(qpe), ckv, kpe, sc, i32_dev(table), i32_dev(inp["seq_lens"]), G, ws, o_a, lse_a)
+    o_b, lse_b = o_a.clone(), lse_a.clone()
+    wuv = bf16_dev(inp["w_uv"])
+    out_a = torch.empty(B, H, 128, dtype=torch.float32, device="cuda")
+    out_b = torch.full((B, H, 128), float("nan"), dtype=torch.float32, device="cuda")
+    L.mla_split_kv_combine(p, ws, G, o_a, lse_a)
+    L.mla_out_proj(p, o_a, wuv, out_a)
+    L.mla_combine_out_proj(p, ws, G, o_b, wuv, out_b, lse_b)
+    torch.cuda.synchronize()
+    assert L.mla_workspace_status(ws) == 0
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if B * ((H + 7) // 8) >= 2 * sms:
+        assert torch.equal(o_a, o_b) and torch.equal(lse_a, lse_b) and torch.equal(out_a, out_b)
+    else:
+        assert tol_ok(to_f64(out_b), to_f64(out_a), 1e-2, 1e-3)[0]
+        assert tol_ok(to_f64(o_b), to_f64(o_a), 1e-2, 1e-3)[0]
+        assert np.allclose(to_f64(lse_b), to_f64(lse_a), atol=1e-4)
+    pairs = sample_pairs(B, H, 3, 3, seed=7)
+    ref, lse_ref = O.decode_reference(cache, inp, qpe, pairs)
+    got = np.stack([to_f64(out_b[b, h]) for b, h in pairs])
+    ok, err, bound = tol_ok(got, ref, TOL_REL, TOL_ABS)
+    assert ok, (err, bound)
+    assert np.allclose([float(lse_b[b, h]) for b, h in pairs], lse_ref, atol=1e-3)
+
+
 # ------------------------------------------------------------------ FP8 cache
 def test_fp8_cache_small():
     inp = small_inputs([300, 64, 1, 129])
