@@ -28,7 +28,7 @@ sys.path.insert(0, ROOT)
 
 import mla_inputs as mi  # noqa: E402
 
-E2E_STEPS = 8  # steps recorded in one graph by the end-to-end leg
+E2E_STEPS = 32  # steps recorded in one graph by the end-to-end leg
 METRIC = "MLA decode tokens/s and latent-cache HBM GB/s (% of ~8 TB/s roofline), 1 B300"
 FLUSH_BYTES = 256 << 20
 

@@ -106,6 +106,78 @@ __device__ inline float warp_merge_partials(const __nv_bfloat16* __restrict__ pa
   return sum > 0.f ? m + logf(sum) : -INFINITY;
 }
 
+// Two rows at once, each with 2..4 partials (the common case of a batch
+// split across a few workers): the same operations as warp_merge_partials
+// row by row, in the same order (so the same bits), with both rows' loads in
+// flight together.
+__device__ inline void warp_merge_two_small(const __nv_bfloat16* __restrict__ part_o,
+                                            const float* __restrict__ part_lse, const SeqWorkers (&sw)[2], int G,
+                                            int H, int h, float (&acc)[2][16], float (&lse)[2]) {
+  const int lane = threadIdx.x & 31;
+  int sl[2];
+  float l[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    sl[i] = -1;
+    if (lane < sw[i].n) {
+      const int w = sw[i].wf + lane;
+      const long long lo = range_lo(w, G, sw[i].P), hi = range_lo(w + 1, G, sw[i].P);
+      sl[i] = lo == hi ? -1 : (sw[i].sb <= lo ? w : G + w);
+    }
+    l[i] = sl[i] >= 0 ? part_lse[(size_t)sl[i] * H + h] : -INFINITY;
+  }
+  float m[2], wt[2], sum[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    float cm = l[i];
+#pragma unroll
+    for (int o = 16; o; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
+    m[i] = cm;  // the first chunk: nothing to rescale
+    wt[i] = l[i] == -INFINITY ? 0.f : __expf(l[i] - m[i]);
+    float ws = wt[i];
+#pragma unroll
+    for (int o = 16; o; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
+    sum[i] = 0.f + ws;
+  }
+  uint4 v[2][4][2];
+  float wk[2][4];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int slk = __shfl_sync(0xffffffffu, sl[i], u);
+      wk[i][u] = __shfl_sync(0xffffffffu, wt[i], u);
+      if (u < sw[i].n && slk >= 0) {
+        const uint4* src = reinterpret_cast<const uint4*>(part_o + ((size_t)slk * H + h) * kLatent) + 2 * lane;
+        v[i][u][0] = src[0];
+        v[i][u][1] = src[1];
+      } else {
+        v[i][u][0] = v[i][u][1] = make_uint4(0, 0, 0, 0);
+        wk[i][u] = 0.f;
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+#pragma unroll
+    for (int k = 0; k < 16; ++k) acc[i][k] = 0.f;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint32_t w8[8] = {v[i][u][0].x, v[i][u][0].y, v[i][u][0].z, v[i][u][0].w,
+                              v[i][u][1].x, v[i][u][1].y, v[i][u][1].z, v[i][u][1].w};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        acc[i][2 * e] = fmaf(wk[i][u], bf16lo(w8[e]), acc[i][2 * e]);
+        acc[i][2 * e + 1] = fmaf(wk[i][u], bf16hi(w8[e]), acc[i][2 * e + 1]);
+      }
+    }
+    const float inv = sum[i] > 0.f ? 1.f / sum[i] : 0.f;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) acc[i][k] *= inv;
+    lse[i] = sum[i] > 0.f ? m[i] + logf(sum[i]) : -INFINITY;
+  }
+}
+
 // acc (16 fp32, lane l's columns) as 8 bf16 pairs.
 __device__ inline void pack_row16(const float (&acc)[16], uint32_t (&o8)[8]) {
 #pragma unroll

@@ -196,8 +196,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   const uint32_t full = smem_u32(&bars[0]), empty = smem_u32(&bars[kMaxS]), done = smem_u32(&bars[2 * kMaxS]);
   const uint32_t ncols = g.N <= 32 ? 32 : g.N <= 64 ? 64 : 128;
 
+  // W_UV does not depend on the preceding kernels: the set-up and the
+  // weight's first S K blocks go out before the dependency wait, while the
+  // decode's last clusters finish
   if (threadIdx.x == 32) prefetch_l2(g.weight + (size_t)h * kV * kLatent, kV * kLatent * 2);
-  grid_dep_wait();  // the decode's o_lat and partials
   if (threadIdx.x == 0) {
     abort_flag = 0;
     for (int i = 0; i < S; ++i) {
@@ -212,14 +214,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     tmem_alloc(smem_u32(&tmem_slot), ncols);
     tmem_relinquish();
   }
-  if (threadIdx.x >= 64 && threadIdx.x - 64 < g.N && nt * g.N + (int)threadIdx.x - 64 < g.B)
-    s_sw[threadIdx.x - 64] = seq_workers(g.seq_start, g.B, g.G, nt * g.N + (int)threadIdx.x - 64);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
-
-  // the weight's first S K blocks in flight before the combine work
   int issued = 0;  // (producer thread)
   auto issue = [&](int kb) {
     const int s = kb % S;
@@ -231,27 +229,44 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   if (warp == 0 && lane == 0)
     for (int kb = 0; kb < S && kb < KB; ++kb) issue(kb);
 
-  // B operand rows: warp w takes rows w, w + 8, ...; lane l holds latent
-  // columns [16 l, 16 l + 16), i.e. 16-byte chunks 2(l%4), 2(l%4)+1 of K block l/4
-  for (int r = warp; r < g.N; r += kFusedThreads / 32) {
+  grid_dep_wait();  // the decode's o_lat and partials
+  if (threadIdx.x >= 64 && threadIdx.x - 64 < g.N && nt * g.N + (int)threadIdx.x - 64 < g.B)
+    s_sw[threadIdx.x - 64] = seq_workers(g.seq_start, g.B, g.G, nt * g.N + (int)threadIdx.x - 64);
+  __syncthreads();
+
+  // B operand rows: warp w takes rows w + 32 k and w + 32 k + 16; lane l
+  // holds latent columns [16 l, 16 l + 16), i.e. 16-byte chunks 2(l%4),
+  // 2(l%4)+1 of K block l/4.  Two rows split over 2..4 workers are merged
+  // together (their loads in flight at once), any other row on its own.
+  auto small_split = [&](int r) {
+    return r < g.N && nt * g.N + r < g.B && s_sw[r].n >= 2 && s_sw[r].n <= 4;
+  };
+  auto write_merged = [&](int r, const float (&acc)[16], float l, uint32_t (&o8)[8]) {
     const int b = nt * g.N + r;
-    uint32_t o8[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    if (b < g.B) {
-      const SeqWorkers sw = s_sw[r];
-      uint4* row = reinterpret_cast<uint4*>(g.o_lat + ((size_t)b * g.H + h) * kLatent) + 2 * lane;
-      if (sw.n <= 1) {  // finished by the decode (or empty)
-        const uint4 v0 = row[0], v1 = row[1];
-        o8[0] = v0.x; o8[1] = v0.y; o8[2] = v0.z; o8[3] = v0.w;
-        o8[4] = v1.x; o8[5] = v1.y; o8[6] = v1.z; o8[7] = v1.w;
-      } else {
-        float acc[16];
-        const float l = warp_merge_partials(g.part_o, g.part_lse, sw, g.G, g.H, h, acc);
-        pack_row16(acc, o8);
-        row[0] = make_uint4(o8[0], o8[1], o8[2], o8[3]);
-        row[1] = make_uint4(o8[4], o8[5], o8[6], o8[7]);
-        if (lane == 0 && g.lse) g.lse[(size_t)b * g.H + h] = l;
-      }
+    pack_row16(acc, o8);
+    uint4* row = reinterpret_cast<uint4*>(g.o_lat + ((size_t)b * g.H + h) * kLatent) + 2 * lane;
+    row[0] = make_uint4(o8[0], o8[1], o8[2], o8[3]);
+    row[1] = make_uint4(o8[4], o8[5], o8[6], o8[7]);
+    if (lane == 0 && g.lse) g.lse[(size_t)b * g.H + h] = l;
+  };
+  auto one_row = [&](int r, uint32_t (&o8)[8]) {
+    const int b = nt * g.N + r;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o8[e] = 0;
+    if (b >= g.B) return;
+    const SeqWorkers sw = s_sw[r];
+    if (sw.n <= 1) {  // finished by the decode (or empty)
+      const uint4* row = reinterpret_cast<const uint4*>(g.o_lat + ((size_t)b * g.H + h) * kLatent) + 2 * lane;
+      const uint4 v0 = row[0], v1 = row[1];
+      o8[0] = v0.x; o8[1] = v0.y; o8[2] = v0.z; o8[3] = v0.w;
+      o8[4] = v1.x; o8[5] = v1.y; o8[6] = v1.z; o8[7] = v1.w;
+    } else {
+      float acc[16];
+      const float l = warp_merge_partials(g.part_o, g.part_lse, sw, g.G, g.H, h, acc);
+      write_merged(r, acc, l, o8);
     }
+  };
+  auto store_row = [&](int r, const uint32_t (&o8)[8]) {
     const uint32_t blk = bbase + (uint32_t)(lane >> 2) * bblk + (uint32_t)r * 128u;
     const uint32_t c0 = 2u * (lane & 3);
     asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(blk + ((c0 ^ (r & 7)) << 4)), "r"(o8[0]), "r"(o8[1]),
@@ -260,6 +275,22 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(blk + (((c0 + 1) ^ (r & 7)) << 4)), "r"(o8[4]),
                  "r"(o8[5]), "r"(o8[6]), "r"(o8[7])
                  : "memory");
+  };
+  for (int r0 = warp; r0 < g.N; r0 += 2 * (kFusedThreads / 32)) {
+    const int r1 = r0 + kFusedThreads / 32;
+    uint32_t o8[2][8];
+    if (small_split(r0) && small_split(r1)) {
+      const SeqWorkers sw2[2] = {s_sw[r0], s_sw[r1]};
+      float acc[2][16], l[2];
+      warp_merge_two_small(g.part_o, g.part_lse, sw2, g.G, g.H, h, acc, l);
+      write_merged(r0, acc[0], l[0], o8[0]);
+      write_merged(r1, acc[1], l[1], o8[1]);
+    } else {
+      one_row(r0, o8[0]);
+      if (r1 < g.N) one_row(r1, o8[1]);
+    }
+    store_row(r0, o8[0]);
+    if (r1 < g.N) store_row(r1, o8[1]);
   }
   fence_proxy_async_smem();  // the B operand, for the tensor cores
   __syncthreads();
