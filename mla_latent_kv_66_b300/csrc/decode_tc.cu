@@ -105,6 +105,7 @@ constexpr float kRescaleLog2 = 8.f;  // lazy rescale threshold: P stays <= 2^8
 // the 14 octaves below the running maximum.
 constexpr float kRescaleLog2_8 = 2.f, kPShift8 = 6.f;
 constexpr int kIdRing = 16;          // page ids read ahead by the producer
+constexpr int kPreIssue = 1;         // stage loads issued before the start-up barrier
 
 enum {
   B_FULL = 0,                       // bf16 stage ready (TMA landed, or E4M3 expanded)
@@ -495,9 +496,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < kIdRing; ++i) page_ids[i] = v[i];
       id_count = kIdRing;
-      // the ring's first pages need no free slot; their ids are all loaded,
-      // so the read-ahead of further ids starts after the start-up barrier
-      for (; pit.have && g_prod < (uint32_t)kRing; ++g_prod) {
+      // the first page needs no free slot and its id is loaded; the read-ahead
+      // of further ids starts after the start-up barrier
+      for (; pit.have && g_prod < (uint32_t)min(kPreIssue, kRing); ++g_prod) {
         issue(g_prod);
         pit.advance(a);
       }
@@ -537,6 +538,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const int free_bar = kFp8 ? B_RFREE : B_EMPTY, full_bar = kFp8 ? B_RFULL : B_FULL;
       bool ok = true;
+      // the rest of the ring waits for the first unit's query: its loads
+      // would otherwise queue behind every CTA's stage loads
+      if (pit.have && !mbar_wait(bar(B_QFULL), 0, &abort_flag, a.err)) ok = false;
       for (; ok && pit.have; ++g_prod) {
         const uint32_t s = g_prod % kRing;
         if (g_prod >= (uint32_t)kRing &&
