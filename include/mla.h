@@ -344,6 +344,18 @@ mla_status mla_decode_static_status(int clear, mla_stream_t stream);
  * is non-zero. */
 mla_status mla_workspace_status(void* workspace, int clear, mla_stream_t stream);
 
+/* ---------------------------------------------------------------------
+ * mla_selftest_bounded_wait: diagnostic of the kernels' bounded waits (not a
+ * step of the method).  Every mbarrier wait in the library's kernels gives up
+ * after 2 s of global time, records MLA_ERR_TIMEOUT in the workspace's error
+ * word and lets the kernel return.  This call launches one block that waits
+ * on an mbarrier nothing completes; after the limit the error word of
+ * `workspace` (4 bytes at offset 0, zeroed by the caller) holds
+ * MLA_ERR_TIMEOUT (read it with mla_workspace_status) and the stream goes
+ * on.  The kernel takes about 2 s.
+ */
+mla_status mla_selftest_bounded_wait(void* workspace, mla_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

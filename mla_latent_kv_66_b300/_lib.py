@@ -70,6 +70,7 @@ _SIGS = {
     "mla_multi_token_expand": (ctypes.c_int, [ctypes.POINTER(MlaParams), ctypes.c_int, _P, _P, _P, _P, _P]),
     "mla_decode_static": (ctypes.c_int, [ctypes.POINTER(MlaParams), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "mla_decode_static_status": (ctypes.c_int, [ctypes.c_int, _P]),
+    "mla_selftest_bounded_wait": (ctypes.c_int, [_P, _P]),
 }
 
 
@@ -196,3 +197,7 @@ def mla_multi_token_expand(p, q_len, page_table, seq_lens, page_table_out, seq_l
     length seq_lens[b] - q_len + 1 + i (p.B = number of sequences)."""
     _check(lib.mla_multi_token_expand(ctypes.byref(p), q_len, _ptr(page_table), _ptr(seq_lens), _ptr(page_table_out),
                                       _ptr(seq_lens_out), _stream(stream)), "mla_multi_token_expand")
+
+
+def mla_selftest_bounded_wait(workspace, stream=None):
+    _check(lib.mla_selftest_bounded_wait(_ptr(workspace), _stream(stream)), "mla_selftest_bounded_wait")

@@ -279,6 +279,26 @@ def test_host_rejects_bad_arguments_with_an_error():
         L.mla_out_proj(p, x, x, None)
 
 
+# ------------------------------------------------------------------ bounded waits
+def test_a_wait_that_never_completes_ends_with_a_timeout_status():
+    """The library's bounded mbarrier wait on a barrier nothing completes:
+    after its limit the kernel records MLA_ERR_TIMEOUT and returns, and the
+    context stays usable (a decode runs correctly right after)."""
+    import time
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    t0 = time.perf_counter()
+    L.mla_selftest_bounded_wait(ws)
+    assert L.mla_workspace_status(ws) == L.MLA_ERR_TIMEOUT
+    assert time.perf_counter() - t0 >= 1.5
+    inp = small_inputs([130, 64])
+    cache = O.build_cache(inp)
+    qpe = O.rope_q_bf16(inp["q_pe_raw"], inp["seq_lens"])
+    r = run_gpu(inp, cache, qpe, 2)
+    assert r["status"] == 0
+    ref, _ = oracle_all(inp, cache, qpe)
+    assert tol_ok(to_f64(r["out"]).reshape(-1, 128), ref, TOL_REL, TOL_ABS)[0]
+
+
 # ------------------------------------------------------------------ combine fused into the out-projection
 @pytest.mark.parametrize("lens,G,H", [([700, 64, 1, 130, 65, 2000], 7, 16), ([4096] * 32, 0, 128),
                                       ([1500] * 40, 64, 128)])

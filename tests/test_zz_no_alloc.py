@@ -25,15 +25,15 @@ pytestmark = pytest.mark.gpu
 TOL_REL, TOL_ABS = 1e-2, 1e-3
 
 
-def _inputs(lens, H, seed):
+def _inputs(lens, H, seed, kv="bf16"):
     w = mi.Workload("static", B=len(lens), H=H, L=0, ragged=(1, 2), seed=seed, pages="permuted")
     inp = mi.make_inputs(w, with_kv=False)
     inp["seq_lens"] = np.asarray(lens, np.int32)
     inp["page_table"], inp["num_pages"] = mi.page_layout(w, inp["seq_lens"])
     inp["kv_raw"] = {b: mi.kv_rows(w, b, int(lens[b])) for b in range(len(lens))}
-    cache = O.build_cache(inp)
+    cache = O.build_cache(inp, "bf16" if kv == "bf16" else "e4m3")
     dev = dict(
-        p=L.make_params(len(lens), H, inp["page_table"].shape[1], inp["num_pages"]),
+        p=L.make_params(len(lens), H, inp["page_table"].shape[1], inp["num_pages"], kv),
         q_lat=bf16_dev(O.f64_to_bf16(O.absorb_q(inp["q_nope"], inp["w_uk"]))),
         q_pe=bf16_dev(O.rope_q_bf16(inp["q_pe_raw"], inp["seq_lens"])),
         table=i32_dev(inp["page_table"]), lens=i32_dev(inp["seq_lens"]))
@@ -58,6 +58,19 @@ def _static(d):
     lse = torch.full((p.B, p.H), float("nan"), dtype=torch.float32, device="cuda")
     L.mla_decode_static(p, d["q_lat"], d["q_pe"], d["ckv"], d["kpe"], d["sc"], d["table"], d["lens"], o, lse)
     return o, lse
+
+
+@pytest.mark.parametrize("kv", ["e4m3", "e4m3_mma"])
+def test_static_scratch_with_an_e4m3_cache(kv):
+    """The E4M3 caches through the fixed scratch (the tensor-core mode keeps
+    its E4M3 query there too): bit-equal to the workspace entry points."""
+    for d in (_inputs([1500, 64, 1, 300], H=128, seed=33, kv=kv), _inputs([900, 2500], H=128, seed=34, kv=kv)):
+        o_ref, lse_ref = _with_workspace(d)
+        o, lse = _static(d)
+        torch.cuda.synchronize()
+        assert L.mla_decode_static_status() == L.MLA_OK
+        assert torch.equal(o.view(torch.int16), o_ref.view(torch.int16))
+        assert torch.equal(lse, lse_ref)
 
 
 def test_static_scratch_matches_the_workspace_entry_point_on_two_calls():
