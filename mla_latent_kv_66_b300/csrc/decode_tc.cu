@@ -88,7 +88,7 @@ struct Layout {
   static constexpr uint32_t kOffX = kOffQpe + 8192;                // the peer's partial score tile
   static constexpr uint32_t kOffXs = kOffX + kXBytes;              // own partial, outgoing
   static constexpr uint32_t kSmemBytes = kOffXs + kXBytes + 1024;
-  static constexpr uint32_t kStaticSmem = kMma8 ? 7 * 1024 : 4 * 1024;  // static shared memory, rounded up
+  static constexpr uint32_t kStaticSmem = kMma8 ? 8 * 1024 : 4 * 1024;  // static shared memory, rounded up
   static_assert(kStageBytes % 1024 == 0 && kRawBytes % 128 == 0 && kOffQpe % 512 == 0,
                 "swizzled tiles need 1024-byte (128 B swizzle) / 512-byte (64 B, 32 B) alignment");
   static_assert(kStages <= kMaxStages, "stage barriers");
@@ -379,10 +379,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   __shared__ uint32_t lsum_swap[2 * 128];  // row sums between them at the end of a unit
   __shared__ int page_ids[kIdRing];        // producer-private
   __shared__ int sl_cache[32];             // lengths of the range's first sequences
-  // 8-bit mode: log2 of the current page's token scales (one copy per
-  // exchange warp) and their reciprocals for the softmax (by page parity and
-  // row quarter; 0 past the sequence end)
-  __shared__ __align__(16) float tok_lg[kF8 ? 4 * 64 : 1];  // read as float4
+  // 8-bit mode: log2 of a page's token scales and their reciprocals, for the
+  // softmax (by page parity and row quarter; 0 past the sequence end)
+  __shared__ __align__(16) float tok_lg[kF8 ? 2 * 4 * 64 : 1];
   __shared__ __align__(16) float tok_inv[kF8 ? 2 * 4 * 64 : 1];
 
   const uint32_t rank = cluster_rank(), peer = rank ^ 1u;
@@ -801,46 +800,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (!wwait(B_SFULL, g & 1)) { ok = false; break; }
         tc_fence_after();
         const float* tsc = reinterpret_cast<const float*>(smem_base + (g % kStages) * kStageBytes + kStageScale);
-        float* lg = tok_lg + q4 * 64;
-        if constexpr (kF8) {
-          // the score of token t is q_scale * scale_t times the score of the
-          // codes; rank 0 also adds log2(scale_t), which carries the token
-          // scale into the probabilities (P . V multiplies codes)
-          lg[lane] = rank == 0 ? __log2f(tsc[lane]) : 0.f;
-          lg[lane + 32] = rank == 0 ? __log2f(tsc[lane + 32]) : 0.f;
-          __syncwarp();
-        }
+        // 8-bit mode: the score of the codes times the query row's scale; the
+        // softmax multiplies the sum of both partials by the token scale
+        const float cq = kF8 ? c * qs_cur : c;
         float v[64];
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           uint32_t s32[32];
           tmem_ld32(tmem + lane_base + kTmS + half * 32, s32);
           tmem_wait_ld();
-          if constexpr (kF8) {
-            const float cq = c * qs_cur;
-            const float4* t4 = reinterpret_cast<const float4*>(tsc) + half * 8;
-            const float4* l4 = reinterpret_cast<const float4*>(lg) + half * 8;
 #pragma unroll
-            for (int c4 = 0; c4 < 8; ++c4) {
-              const float4 f = t4[c4], o = l4[c4];
-              const int k = half * 32 + 4 * c4;
-              v[k] = fmaf(__uint_as_float(s32[4 * c4]), cq * f.x, o.x);
-              v[k + 1] = fmaf(__uint_as_float(s32[4 * c4 + 1]), cq * f.y, o.y);
-              v[k + 2] = fmaf(__uint_as_float(s32[4 * c4 + 2]), cq * f.z, o.z);
-              v[k + 3] = fmaf(__uint_as_float(s32[4 * c4 + 3]), cq * f.w, o.w);
-            }
-          } else {
-#pragma unroll
-            for (int k = 0; k < 32; ++k) v[half * 32 + k] = __uint_as_float(s32[k]) * c;
-          }
+          for (int k = 0; k < 32; ++k) v[half * 32 + k] = __uint_as_float(s32[k]) * cq;
         }
         tc_fence_before();
         mbar_arrive(bar(B_SFREE));
-        float inv_a = 0.f, inv_b = 0.f;
+        float inv_a = 0.f, inv_b = 0.f, lg_a = 0.f, lg_b = 0.f;
         if constexpr (kF8) {
+          // for the softmax: log2(scale_t), which carries the token scale into
+          // the probabilities (P . V multiplies codes), and 1 / scale_t for
+          // the row sums (0 past the sequence end)
           const int nv = min(kPage, u.n - jp * kPage);
           inv_a = lane < nv ? __frcp_rn(tsc[lane]) : 0.f;
           inv_b = lane + 32 < nv ? __frcp_rn(tsc[lane + 32]) : 0.f;
+          lg_a = lane < nv ? __log2f(tsc[lane]) : 0.f;
+          lg_b = lane + 32 < nv ? __log2f(tsc[lane + 32]) : 0.f;
         }
         if constexpr (kFp8) {
           // E4M3: the score of token t is scale_t times the score of its codes
@@ -867,6 +850,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           float* inv = tok_inv + ((g & 1) * 4 + q4) * 64;
           inv[lane] = inv_a;
           inv[lane + 32] = inv_b;
+          float* lg = tok_lg + ((g & 1) * 4 + q4) * 64;
+          lg[lane] = lg_a;
+          lg[lane + 32] = lg_b;
         }
         uint8_t* xt = smem_base + kOffXs;
 #pragma unroll
@@ -981,6 +967,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         mbar_arrive(bar(B_XREAD + q4));  // the exchange warp of this quarter tells the peer
         const uint32_t sca = base + s * kStageBytes + kStageScale + j * 128;  // E4M3 token scales
+        if constexpr (kF8) {
+          // the token scale: on the score, and as log2(scale_t) into P
+          const float4* ts4 = reinterpret_cast<const float4*>(smem_base + s * kStageBytes + kStageScale) + 8 * j;
+          const float4* lg4 = reinterpret_cast<const float4*>(tok_lg + ((gi & 1) * 4 + q4) * 64 + 32 * j);
+#pragma unroll
+          for (int c4 = 0; c4 < 8; ++c4) {
+            const float4 f = ts4[c4], o = lg4[c4];
+            x[4 * c4] = fmaf(x[4 * c4], f.x, o.x);
+            x[4 * c4 + 1] = fmaf(x[4 * c4 + 1], f.y, o.y);
+            x[4 * c4 + 2] = fmaf(x[4 * c4 + 2], f.z, o.z);
+            x[4 * c4 + 3] = fmaf(x[4 * c4 + 3], f.w, o.w);
+          }
+        }
         if constexpr (kFp8) {
           if (!wwait(B_FULL + s, (gi / kStages) & 1)) { ok = false; break; }  // scales visible
         }
@@ -1011,7 +1010,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         float ps[4] = {0.f, 0.f, 0.f, 0.f};
         uint32_t pk[16];
         if constexpr (kF8) {
-          // x carries log2(scale_t) (added by rank 0), so P = 2^(x - mm) is
+          // x carries log2(scale_t) (added above), so P = 2^(x - mm) is
           // the probability times the token scale, as P . V on the codes needs
           // it; the row sum takes P / scale_t.  P becomes E4M3 terms: hi is P
           // rounded to 4 significant bits (half up; exact in E4M3's normal
