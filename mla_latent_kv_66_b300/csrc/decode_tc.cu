@@ -1,28 +1,34 @@
-// Latent-attention decode on the tcgen05 tensor cores (bf16 latent cache).
+// Latent-attention decode on the tcgen05 tensor cores.
 //
 // Method (mtrt.cn DeepSeek-Coder-V2 MLA page, forward flow; absorbed form):
 //   s_t = scale * (q_lat . c_t + q_pe . k_pe_t),  o_lat = sum_t softmax(s)_t c_t
 // for all H <= 128 heads of one sequence at once: the heads are the M = 128
 // rows of every MMA, so each 64-token cache page is read from HBM once and
-// shared by all heads.
+// shared by all heads.  Three cache modes (template parameter kMode):
+//   0  bf16 cache, kind::f16 MMAs;
+//   1  E4M3 cache + fp32 scale per token, the codes expanded exactly to bf16
+//      in shared memory by the exchange warps, kind::f16 MMAs;
+//   2  the same E4M3 cache multiplied as codes by kind::f8f6f4 MMAs, with the
+//      query and the probabilities as E4M3 terms (hotdry.top DeepSeek-V3.2-Exp
+//      MLA page, deployment paragraph: FP8 when serving).
 //
 // The fp32 latent accumulator O[128 heads x 512] alone needs all 512 tensor
 // memory columns of an SM, so a cluster of two CTAs splits the latent axis
 // and the shared RoPE key evenly:
 //   rank 0: latent columns [0,256), k_pe [0,32);
 //   rank 1: latent columns [256,512), k_pe [32,64).
-// Each CTA TMA-loads only its part of every page (36 KB of the 72 KB) and
-// computes the partial score over its 288 of the 576 dimensions.  The two
-// fp32 partial score tiles (log2 domain) are swapped through distributed
-// shared memory by the async copy engine; each CTA adds its own partial to
-// the peer's, so both add the same two numbers exactly and take the same
-// softmax decisions.  Each CTA then accumulates P . c over its own 256 latent
-// columns.
+// Each CTA TMA-loads only its part of every page and computes the partial
+// score over its 288 of the 576 dimensions.  The two fp32 partial score tiles
+// (log2 domain) are swapped through distributed shared memory by the async
+// copy engine; each CTA adds its own partial to the peer's, so both add the
+// same two numbers exactly and take the same softmax decisions.  Each CTA
+// then accumulates P . c over its own 256 latent columns.
 //
 // Warp roles (512 threads):
 //   warp 0       KV-partition schedule and the first page ids, then the TMA
-//                producer (cache pages, stage ring); its first loads are
-//                issued before the CTA-wide start-up barrier
+//                producer (cache pages, stage ring); one stage load is issued
+//                before the CTA-wide start-up barrier, the rest of the ring
+//                once the first unit's query is in
 //   warp 1       MMA issuer for S = Q K^T (A = query in tensor memory)
 //   warp 2       tensor-memory allocation
 //   warp 3       split records; then MMA issuer for O += P V (a separate
@@ -34,7 +40,9 @@
 //                on its own: warp q hands quarter q back to the peer as soon
 //                as its two softmax warps have read it); load each unit's
 //                query into tensor memory as soon as the previous unit's last
-//                S = Q K^T is done; E4M3 cache: expand the codes
+//                S = Q K^T is done; mode 1: expand the codes; mode 2: load the
+//                first unit's query too, publish each page's token-scale
+//                logarithms and reciprocals
 //   warps 8..15  two softmax warpgroups; warpgroup j owns tokens [32j, 32j+32)
 //                of every page, thread = head row: own staged partial + the
 //                peer's, row maximum agreed with the other warpgroup, online
@@ -42,7 +50,7 @@
 //                (two P buffers), its half of O rescaled when needed and
 //                written at the end of a unit.
 // Tensor memory: O [0,256), S [256,320), P double buffer [320,384) (bf16
-// pairs, the A operand of P . V), query [384,512).
+// pairs, or E4M3 terms), query [384,512).
 #include <cuda_fp16.h>
 
 #include "kernels.h"
