@@ -190,7 +190,7 @@ def setup_gpu(w, device):
     step = mla.MLADecodeStep(w.B, w.H, table.shape[1], npg, w.kv_dtype, w.out_dtype, w.splits, device,
                              q_len=w.q_len)
     # rows of the step: the sequences, or q_len rows per sequence (the page
-    # table and lengths the four calls see; the query is rotated at each
+    # table and lengths the calls see; the query is rotated at each
     # row's length minus one)
     rows_table, rows_lens = step.expand_rows(table_d, lens_d)
     q_pe = torch.empty(w.B * w.q_len, w.H, 64, dtype=torch.bfloat16, device=device)

@@ -90,7 +90,7 @@ const char* mla_status_string(mla_status s) {
   return "unknown status";
 }
 
-int mla_version(void) { return 100; }
+int mla_version(void) { return 200; }
 
 int mla_decode_num_splits(const mla_params* p, int num_splits) {
   if (check_params(p) != MLA_OK) return -1;

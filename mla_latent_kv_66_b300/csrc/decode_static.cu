@@ -12,8 +12,8 @@
 
 namespace {
 
-// Scratch for the error word, split records, sequence page offsets and the
-// split-KV partial results.  Every GPU that loads the library holds it until
+// Scratch for the error word, split records, sequence page offsets, the
+// split-KV partial results and (8-bit tensor-core modes) the E4M3 query.  Every GPU that loads the library holds it until
 // the process exits.  Every call shares it.
 constexpr size_t kStaticWsBytes = 32u << 20;
 static __device__ __align__(256) uint8_t g_static_ws[kStaticWsBytes];

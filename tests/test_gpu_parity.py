@@ -481,7 +481,7 @@ def run_multi(inp, cache, q_pe_bits, T, num_splits=0):
 
 def test_multi_token_decode_against_the_oracle():
     """Three query tokens per sequence with a causal mask, through the row
-    expansion and the four calls: every (sequence, token, head) against the
+    expansion and the decode step: every (sequence, token, head) against the
     oracle, including a sequence exactly as long as the query block; the
     expanded page table and lengths bit-exact; the GPU query rotation at the
     expanded lengths within one bf16 ulp of the oracle's."""
