@@ -345,6 +345,29 @@ def test_combine_fused_into_out_projection(lens, G, H):
     assert np.allclose([float(lse_b[b, h]) for b, h in pairs], lse_ref, atol=1e-3)
 
 
+def test_batch_larger_than_one_gemm_tile():
+    """B = 300 short sequences through the decode step: the absorption
+    (batch tiles of up to 256) and the fused combine + out-projection (tiles
+    of up to 128) each run several batch tiles; sampled outputs of every
+    tile against the oracle."""
+    rng = np.random.default_rng(41)
+    lens = rng.integers(1, 300, size=300).tolist()
+    inp = small_inputs(lens, H=16, seed=43)
+    cache = O.build_cache(inp, garbage=garbage(inp))
+    qpe = O.rope_q_bf16(inp["q_pe_raw"], inp["seq_lens"])
+    B, table = len(lens), inp["page_table"]
+    step = mla.MLADecodeStep(B, 16, table.shape[1], inp["num_pages"])
+    out = step(bf16_dev(inp["q_nope"]), bf16_dev(qpe), bf16_dev(inp["w_uk"]), bf16_dev(inp["w_uv"]),
+               *upload_cache(cache), i32_dev(table), i32_dev(inp["seq_lens"]))
+    torch.cuda.synchronize()
+    assert step.status() == 0
+    pairs = [(b, h) for b in (0, 127, 128, 200, 255, 256, 299) for h in (0, 9, 15)]
+    ref, _ = O.decode_reference(cache, inp, qpe, pairs)
+    got = np.stack([to_f64(out[b, h]) for b, h in pairs])
+    ok, err, bound = tol_ok(got, ref, TOL_REL, TOL_ABS)
+    assert ok, (err, bound)
+
+
 # ------------------------------------------------------------------ FP8 cache
 def test_fp8_cache_small():
     inp = small_inputs([300, 64, 1, 129])
