@@ -108,14 +108,17 @@ __device__ inline float warp_merge_partials(const __nv_bfloat16* __restrict__ pa
 
 // Two rows at once, each with 2..4 partials (the common case of a batch
 // split across a few workers): the same operations as warp_merge_partials
-// row by row, in the same order (so the same bits), with both rows' loads in
-// flight together.
+// row by row, in the same order (so the same bits).  The slots need no
+// loads, so every load of both rows (log-sum-exps and partial rows) is
+// issued before any of them is used: one memory round trip.
 __device__ inline void warp_merge_two_small(const __nv_bfloat16* __restrict__ part_o,
                                             const float* __restrict__ part_lse, const SeqWorkers (&sw)[2], int G,
                                             int H, int h, float (&acc)[2][16], float (&lse)[2]) {
   const int lane = threadIdx.x & 31;
   int sl[2];
   float l[2];
+  uint4 v[2][4][2];
+  bool on[2][4];
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
     sl[i] = -1;
@@ -124,7 +127,22 @@ __device__ inline void warp_merge_two_small(const __nv_bfloat16* __restrict__ pa
       const long long lo = range_lo(w, G, sw[i].P), hi = range_lo(w + 1, G, sw[i].P);
       sl[i] = lo == hi ? -1 : (sw[i].sb <= lo ? w : G + w);
     }
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
     l[i] = sl[i] >= 0 ? part_lse[(size_t)sl[i] * H + h] : -INFINITY;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int slk = __shfl_sync(0xffffffffu, sl[i], u);
+      on[i][u] = u < sw[i].n && slk >= 0;
+      if (on[i][u]) {
+        const uint4* src = reinterpret_cast<const uint4*>(part_o + ((size_t)slk * H + h) * kLatent) + 2 * lane;
+        v[i][u][0] = src[0];
+        v[i][u][1] = src[1];
+      } else {
+        v[i][u][0] = v[i][u][1] = make_uint4(0, 0, 0, 0);
+      }
+    }
   }
   float m[2], wt[2], sum[2];
 #pragma unroll
@@ -139,22 +157,13 @@ __device__ inline void warp_merge_two_small(const __nv_bfloat16* __restrict__ pa
     for (int o = 16; o; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
     sum[i] = 0.f + ws;
   }
-  uint4 v[2][4][2];
   float wk[2][4];
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const int slk = __shfl_sync(0xffffffffu, sl[i], u);
       wk[i][u] = __shfl_sync(0xffffffffu, wt[i], u);
-      if (u < sw[i].n && slk >= 0) {
-        const uint4* src = reinterpret_cast<const uint4*>(part_o + ((size_t)slk * H + h) * kLatent) + 2 * lane;
-        v[i][u][0] = src[0];
-        v[i][u][1] = src[1];
-      } else {
-        v[i][u][0] = v[i][u][1] = make_uint4(0, 0, 0, 0);
-        wk[i][u] = 0.f;
-      }
+      if (!on[i][u]) wk[i][u] = 0.f;
     }
   }
 #pragma unroll

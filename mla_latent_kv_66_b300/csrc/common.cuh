@@ -94,13 +94,20 @@ __device__ inline int warp_incl_scan(int v) {
 }
 
 // Worker range [lo, hi) of flattened pages for worker w of G over P pages.
+// A 64-bit division is a long dependent instruction sequence on the GPU, so
+// the common case (the product fits in 32 bits) divides in 32 bits; both
+// give the same integer (non-negative operands).
 __host__ __device__ inline long long range_lo(int w, int G, long long P) {
+  const unsigned long long prod = (unsigned long long)w * (unsigned long long)P;
+  if (w >= 0 && P >= 0 && prod <= 0xFFFFFFFFull) return (long long)((unsigned)prod / (unsigned)G);
   return (long long)w * P / G;
 }
 
 // Index of the worker whose range holds flattened page x (0 <= x < P).
 __host__ __device__ inline int worker_of(long long x, int G, long long P) {
-  return (int)(((x + 1) * (long long)G - 1) / P);
+  const long long num = (x + 1) * (long long)G - 1;
+  if (num >= 0 && num <= 0xFFFFFFFFll && P > 0 && P <= 0xFFFFFFFFll) return (int)((unsigned)num / (unsigned)P);
+  return (int)(num / P);
 }
 
 // Run by one full warp.  Returns the total page count P and, for flattened

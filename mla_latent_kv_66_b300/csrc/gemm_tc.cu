@@ -319,10 +319,12 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   }
   __syncwarp();
 
-  // epilogue (warps 0-3, one per 32 tensor-memory lanes): thread = v row, columns = batch
-  const bool ok = mbar_wait(done, 0, &abort_flag, nullptr) && !abort_flag;
-  tc_fence_after();
+  // epilogue (warps 0-3, one per 32 tensor-memory lanes): thread = v row,
+  // columns = batch; the other warps go straight to the closing barrier
+  // (fewer threads polling the barrier while the MMAs read shared memory)
   if (warp < 4) {
+    const bool ok = mbar_wait(done, 0, &abort_flag, nullptr) && !abort_flag;
+    tc_fence_after();
     const int row = warp * 32 + lane;
     for (int c0 = 0; c0 < g.N; c0 += 16) {
       uint32_t r[16];
