@@ -269,7 +269,7 @@ def run_ours(args, w, rank, world):
                      G, step.workspace, step.o_lat, step.lse)
         if ev:
             ev[1].record()
-        L.mla_combine_out_proj(p, step.workspace, G, step.o_lat, st["w_uv"], step.out, step.lse)
+        L.mla_combine_out_proj(p, step.workspace, G, st["rows_lens"], step.o_lat, st["w_uv"], step.out, step.lse)
 
     # the step as a CUDA graph (its launches recorded once)
     step.capture(*args_step)

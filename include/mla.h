@@ -236,13 +236,21 @@ mla_status mla_out_proj(const mla_params* p, const void* o_lat, const void* w_uv
  * followed by mla_out_proj whenever mla_split_kv_combine takes its grouped
  * form (B * ceil(H/8) >= 2 x the SM count), and agree to rounding otherwise.
  * Must follow mla_decode on the same stream with the same params,
- * num_splits and workspace.
+ * num_splits, workspace and seq_lens.
+ *   seq_lens : [B] int32 device, the array mla_decode was given, unchanged
+ *           since: the decode's KV partition is a function of the lengths
+ *           alone, so the kernel works out which partials to merge from them
+ *           while the decode is still running (it reads them before waiting
+ *           for the decode to finish)
  *   o_lat : [B,H,512] bf16, read (finished sequences) and written (split
  *           sequences);  lse : [B,H] fp32 or NULL, written for split sequences
  *   w_uv, out : as mla_out_proj
+ * Errors: MLA_ERR_INVALID_ARG for a null seq_lens, o_lat, w_uv or out or a
+ * misaligned pointer; MLA_ERR_WORKSPACE as mla_split_kv_combine.
  */
 mla_status mla_combine_out_proj(const mla_params* p, const void* workspace, size_t ws_bytes, int num_splits,
-                                void* o_lat, float* lse, const void* w_uv, void* out, mla_stream_t stream);
+                                const int32_t* seq_lens, void* o_lat, float* lse, const void* w_uv, void* out,
+                                mla_stream_t stream);
 
 /* ---------------------------------------------------------------------
  * mla_cache_append: write T new tokens into the paged cache (the step before

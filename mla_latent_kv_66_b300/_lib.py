@@ -62,7 +62,7 @@ _SIGS = {
                                             _P, _P, _P]),
     "mla_out_proj": (ctypes.c_int, [ctypes.POINTER(MlaParams), _P, _P, _P, _P]),
     "mla_combine_out_proj": (ctypes.c_int, [ctypes.POINTER(MlaParams), _P, ctypes.c_size_t, ctypes.c_int, _P, _P,
-                                            _P, _P, _P]),
+                                            _P, _P, _P, _P]),
     "mla_cache_append": (ctypes.c_int, [ctypes.POINTER(MlaParams), _P, _P, _P, ctypes.c_int, ctypes.c_int,
                                         _P, _P, _P, _P]),
     "mla_rope_q": (ctypes.c_int, [ctypes.POINTER(MlaParams), _P, _P, _P, _P]),
@@ -157,9 +157,9 @@ def mla_out_proj(p, o_lat, w_uv, out, stream=None):
            "mla_out_proj")
 
 
-def mla_combine_out_proj(p, workspace, num_splits, o_lat, w_uv, out, lse=None, stream=None):
+def mla_combine_out_proj(p, workspace, num_splits, seq_lens, o_lat, w_uv, out, lse=None, stream=None):
     _check(lib.mla_combine_out_proj(ctypes.byref(p), _ptr(workspace),
-                                    workspace.numel() * workspace.element_size(), num_splits,
+                                    workspace.numel() * workspace.element_size(), num_splits, _ptr(seq_lens),
                                     _ptr(o_lat), _ptr(lse), _ptr(w_uv), _ptr(out), _stream(stream)),
            "mla_combine_out_proj")
 

@@ -212,10 +212,11 @@ mla_status mla_split_kv_combine(const mla_params* p, const void* workspace, size
 }
 
 mla_status mla_combine_out_proj(const mla_params* p, const void* workspace, size_t ws_bytes, int num_splits,
-                                void* o_lat, float* lse, const void* w_uv, void* out, mla_stream_t stream) {
+                                const int32_t* seq_lens, void* o_lat, float* lse, const void* w_uv, void* out,
+                                mla_stream_t stream) {
   mla_status s = check_params(p);
   if (s != MLA_OK) return s;
-  if (!o_lat || !w_uv || !out || !aligned16(o_lat) || !aligned16(workspace) || !aligned16(w_uv))
+  if (!seq_lens || !o_lat || !w_uv || !out || !aligned16(o_lat) || !aligned16(workspace) || !aligned16(w_uv))
     return MLA_ERR_INVALID_ARG;
   const int G = resolve_splits(p, num_splits);
   if (G < 1) return MLA_ERR_INVALID_ARG;
@@ -223,9 +224,8 @@ mla_status mla_combine_out_proj(const mla_params* p, const void* workspace, size
   if (!workspace || ws_bytes < l.total) return MLA_ERR_WORKSPACE;
   const uint8_t* ws = static_cast<const uint8_t*>(workspace);
   return cuda_status(launch_outproj_combine(reinterpret_cast<const __nv_bfloat16*>(ws + l.part_o),
-                                            reinterpret_cast<const float*>(ws + l.part_lse),
-                                            reinterpret_cast<const int*>(ws + l.seq_start),
-                                            static_cast<__nv_bfloat16*>(o_lat), lse,
+                                            reinterpret_cast<const float*>(ws + l.part_lse), seq_lens,
+                                            p->max_pages_per_seq, static_cast<__nv_bfloat16*>(o_lat), lse,
                                             static_cast<const __nv_bfloat16*>(w_uv), out,
                                             p->out_dtype == MLA_OUT_BF16, p->B, p->H, G, (cudaStream_t)stream));
 }

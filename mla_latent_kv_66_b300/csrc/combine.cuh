@@ -13,7 +13,7 @@ namespace mla {
 
 // The decode workers whose page ranges overlap sequence b (seq_start: the
 // batch's page offsets, B+1 entries): the first one and their number (0 for
-// an empty sequence).  One thread; 64-bit divisions.
+// an empty sequence).  One thread.
 struct SeqWorkers {
   int wf, n;
   long long sb, P;
@@ -32,27 +32,50 @@ __device__ inline SeqWorkers seq_workers(const int* seq_start, int B, int G, int
   return s;
 }
 
+// Slot of partial i of a split sequence: the worker's first-unit record if
+// its range starts in the sequence, else its last-unit record; -1 for an
+// empty worker range (it wrote none).
+__device__ inline int partial_slot(const SeqWorkers& sw, int G, int i) {
+  const int w = sw.wf + i;
+  const long long lo = range_lo(w, G, sw.P), hi = range_lo(w + 1, G, sw.P);
+  return lo == hi ? -1 : (sw.sb <= lo ? w : G + w);
+}
+
+// Run by one full warp, reading only the sequence lengths (the page counts
+// of the decode's schedule, seq_pages): the batch's total page count, and
+// for sequences [b0, b0 + nrows) their first flattened page (sb) and page
+// count (np), in shared or global memory.
+__device__ inline long long warp_page_offsets(const int32_t* __restrict__ seq_lens, int B, int maxp, int b0,
+                                              int nrows, long long* sb, int* np_out) {
+  const int lane = threadIdx.x & 31;
+  long long run = 0;
+  for (int base = 0; base < B; base += 32) {
+    const int b = base + lane;
+    const int np = b < B ? seq_pages(__ldg(seq_lens + b), maxp, nullptr) : 0;
+    const int incl = warp_incl_scan(np);
+    if (b >= b0 && b < b0 + nrows && b < B) {
+      sb[b - b0] = run + incl - np;
+      np_out[b - b0] = np;
+    }
+    run += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  return run;
+}
+
 // Lane l of the calling warp gets latent columns [16 l, 16 l + 16) of the
 // merged, normalised o (acc) and every lane the merged log-sum-exp.  The
 // partials are taken 32 at a time (slot and lse one per lane) with a running
 // maximum, so each is read once; four partials' loads are kept in flight.
-// Slot of partial i = the worker's first-unit record if its range starts in
-// the sequence, else its last-unit record; an empty worker range wrote none.
 __device__ inline float warp_merge_partials(const __nv_bfloat16* __restrict__ part_o,
                                             const float* __restrict__ part_lse, const SeqWorkers& sw, int G, int H,
                                             int h, float (&acc)[16]) {
   const int lane = threadIdx.x & 31;
-  auto slot_of = [&](int i) {
-    const int w = sw.wf + i;
-    const long long lo = range_lo(w, G, sw.P), hi = range_lo(w + 1, G, sw.P);
-    return lo == hi ? -1 : (sw.sb <= lo ? w : G + w);
-  };
   float m = -INFINITY, sum = 0.f;
 #pragma unroll
   for (int k = 0; k < 16; ++k) acc[k] = 0.f;
   for (int c0 = 0; c0 < sw.n; c0 += 32) {
     const int i = c0 + lane;
-    const int sl = i < sw.n ? slot_of(i) : -1;
+    const int sl = i < sw.n ? partial_slot(sw, G, i) : -1;
     const float l = sl >= 0 ? part_lse[(size_t)sl * H + h] : -INFINITY;
     float cm = l;
 #pragma unroll
@@ -108,33 +131,25 @@ __device__ inline float warp_merge_partials(const __nv_bfloat16* __restrict__ pa
 
 // Two rows at once, each with 2..4 partials (the common case of a batch
 // split across a few workers): the same operations as warp_merge_partials
-// row by row, in the same order (so the same bits).  The slots need no
-// loads, so every load of both rows (log-sum-exps and partial rows) is
-// issued before any of them is used: one memory round trip.
+// row by row, in the same order (so the same bits).  sl[i]: lane u < n[i]
+// holds the slot of partial u of row i (partial_slot), the other lanes -1.
+// Every load of both rows (log-sum-exps and partial rows) is issued before
+// any of them is used: one memory round trip.
 __device__ inline void warp_merge_two_small(const __nv_bfloat16* __restrict__ part_o,
-                                            const float* __restrict__ part_lse, const SeqWorkers (&sw)[2], int G,
-                                            int H, int h, float (&acc)[2][16], float (&lse)[2]) {
+                                            const float* __restrict__ part_lse, const int (&sl)[2],
+                                            const int (&n)[2], int H, int h, float (&acc)[2][16],
+                                            float (&lse)[2]) {
   const int lane = threadIdx.x & 31;
-  int sl[2];
   float l[2];
   uint4 v[2][4][2];
   bool on[2][4];
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    sl[i] = -1;
-    if (lane < sw[i].n) {
-      const int w = sw[i].wf + lane;
-      const long long lo = range_lo(w, G, sw[i].P), hi = range_lo(w + 1, G, sw[i].P);
-      sl[i] = lo == hi ? -1 : (sw[i].sb <= lo ? w : G + w);
-    }
-  }
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
     l[i] = sl[i] >= 0 ? part_lse[(size_t)sl[i] * H + h] : -INFINITY;
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int slk = __shfl_sync(0xffffffffu, sl[i], u);
-      on[i][u] = u < sw[i].n && slk >= 0;
+      on[i][u] = u < n[i] && slk >= 0;
       if (on[i][u]) {
         const uint4* src = reinterpret_cast<const uint4*>(part_o + ((size_t)slk * H + h) * kLatent) + 2 * lane;
         v[i][u][0] = src[0];

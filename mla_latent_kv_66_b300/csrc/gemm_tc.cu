@@ -168,7 +168,8 @@ struct FusedArgs {
   const __nv_bfloat16* weight;  // W_UV, prefetched into L2 before the dependency wait
   const __nv_bfloat16* part_o;
   const float* part_lse;
-  const int* seq_start;
+  const int32_t* seq_lens;  // the lengths mla_decode was given (its schedule is a function of them)
+  int maxp;
   __nv_bfloat16* o_lat;
   float* lse;
   void* out;
@@ -187,6 +188,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
   __shared__ SeqWorkers s_sw[kFusedMaxN];  // the decode workers of each row's sequence
+  __shared__ int s_slot[kFusedMaxN][4];    // and the partial slots of its first four
+  __shared__ long long s_sb[kFusedMaxN];   // first flattened page of each row's sequence
+  __shared__ int s_np[kFusedMaxN];         // and its page count
+  __shared__ long long s_P;                // the batch's page count
 
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t bblk = (uint32_t)g.N * 128u;                 // one K block of the B operand
@@ -196,10 +201,16 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   const uint32_t full = smem_u32(&bars[0]), empty = smem_u32(&bars[kMaxS]), done = smem_u32(&bars[2 * kMaxS]);
   const uint32_t ncols = g.N <= 32 ? 32 : g.N <= 64 ? 64 : 128;
 
-  // W_UV does not depend on the preceding kernels: the set-up and the
-  // weight's first S K blocks go out before the dependency wait, while the
-  // decode's last clusters finish
+  // W_UV and the decode's schedule (a function of the lengths alone) do not
+  // depend on the decode: the set-up, the weight's first S K blocks and each
+  // row's workers and partial slots are done before the dependency wait,
+  // while the decode's last clusters finish
+  const int b0 = nt * g.N, nrows = min(g.N, g.B - b0);
   if (threadIdx.x == 32) prefetch_l2(g.weight + (size_t)h * kV * kLatent, kV * kLatent * 2);
+  if (warp == 3) {
+    const long long P = warp_page_offsets(g.seq_lens, g.B, g.maxp, b0, nrows, s_sb, s_np);
+    if (lane == 0) s_P = P;
+  }
   if (threadIdx.x == 0) {
     abort_flag = 0;
     for (int i = 0; i < S; ++i) {
@@ -228,19 +239,30 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   };
   if (warp == 0 && lane == 0)
     for (int kb = 0; kb < S && kb < KB; ++kb) issue(kb);
-
-  grid_dep_wait();  // the decode's o_lat and partials
-  if (threadIdx.x >= 64 && threadIdx.x - 64 < g.N && nt * g.N + (int)threadIdx.x - 64 < g.B)
-    s_sw[threadIdx.x - 64] = seq_workers(g.seq_start, g.B, g.G, nt * g.N + (int)threadIdx.x - 64);
+  if (threadIdx.x >= 64 && (int)threadIdx.x - 64 < nrows) {
+    const int r = threadIdx.x - 64;
+    SeqWorkers sw;
+    sw.P = s_P;
+    sw.sb = s_sb[r];
+    const long long se = sw.sb + s_np[r];
+    sw.wf = 0;
+    sw.n = 0;
+    if (se > sw.sb) {
+      sw.wf = worker_of(sw.sb, g.G, sw.P);
+      sw.n = worker_of(se - 1, g.G, sw.P) - sw.wf + 1;
+    }
+    s_sw[r] = sw;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) s_slot[r][u] = u < sw.n ? partial_slot(sw, g.G, u) : -1;
+  }
   __syncthreads();
+  grid_dep_wait();  // the decode's o_lat and partials
 
   // B operand rows: warp w takes rows w + 32 k and w + 32 k + 16; lane l
   // holds latent columns [16 l, 16 l + 16), i.e. 16-byte chunks 2(l%4),
   // 2(l%4)+1 of K block l/4.  Two rows split over 2..4 workers are merged
   // together (their loads in flight at once), any other row on its own.
-  auto small_split = [&](int r) {
-    return r < g.N && nt * g.N + r < g.B && s_sw[r].n >= 2 && s_sw[r].n <= 4;
-  };
+  auto small_split = [&](int r) { return r < nrows && s_sw[r].n >= 2 && s_sw[r].n <= 4; };
   auto write_merged = [&](int r, const float (&acc)[16], float l, uint32_t (&o8)[8]) {
     const int b = nt * g.N + r;
     pack_row16(acc, o8);
@@ -280,9 +302,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     const int r1 = r0 + kFusedThreads / 32;
     uint32_t o8[2][8];
     if (small_split(r0) && small_split(r1)) {
-      const SeqWorkers sw2[2] = {s_sw[r0], s_sw[r1]};
+      const int sl2[2] = {lane < 4 ? s_slot[r0][lane] : -1, lane < 4 ? s_slot[r1][lane] : -1};
+      const int n2[2] = {s_sw[r0].n, s_sw[r1].n};
       float acc[2][16], l[2];
-      warp_merge_two_small(g.part_o, g.part_lse, sw2, g.G, g.H, h, acc, l);
+      warp_merge_two_small(g.part_o, g.part_lse, sl2, n2, g.H, h, acc, l);
       write_merged(r0, acc[0], l[0], o8[0]);
       write_merged(r1, acc[1], l[1], o8[1]);
     } else {
@@ -413,9 +436,9 @@ cudaError_t launch_out_proj_tc(const __nv_bfloat16* o_lat, const __nv_bfloat16* 
   return launch_dependent(gemm_tc_kernel<1>, grid, dim3(128), smem, stream, tA, tB, g);
 }
 
-cudaError_t launch_outproj_combine(const __nv_bfloat16* part_o, const float* part_lse, const int* seq_start,
-                                   __nv_bfloat16* o_lat, float* lse, const __nv_bfloat16* w_uv, void* out,
-                                   bool out_bf16, int B, int H, int G, cudaStream_t stream) {
+cudaError_t launch_outproj_combine(const __nv_bfloat16* part_o, const float* part_lse, const int32_t* seq_lens,
+                                   int maxp, __nv_bfloat16* o_lat, float* lse, const __nv_bfloat16* w_uv,
+                                   void* out, bool out_bf16, int B, int H, int G, cudaStream_t stream) {
   if (!aligned16(o_lat) || !aligned16(w_uv) || !aligned16(part_o)) return cudaErrorInvalidValue;
   const int N = std::min(batch_tile(B), kFusedMaxN);
   CUtensorMap tA;
@@ -425,7 +448,7 @@ cudaError_t launch_outproj_combine(const __nv_bfloat16* part_o, const float* par
   // the B operand (N KB) stays; as many weight K blocks in flight as fit
   const size_t bbytes = (size_t)N * 128 * 8;
   const int S = (int)std::min<size_t>(kMaxS, ((200u << 10) - bbytes) / kABytes);
-  FusedArgs g{B, H, N, S, G, w_uv, part_o, part_lse, seq_start, o_lat, lse, out, out_bf16 ? 1 : 0};
+  FusedArgs g{B, H, N, S, G, w_uv, part_o, part_lse, seq_lens, maxp, o_lat, lse, out, out_bf16 ? 1 : 0};
   const size_t smem = S * kABytes + bbytes + 1024;
   cudaError_t e = cudaFuncSetAttribute(outproj_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;

@@ -57,7 +57,7 @@ class MLADecodeStep:
         L.mla_decode(p, self.q_lat, q_pe, ckv, kpe, kv_scale, page_table, seq_lens, G,
                      self.workspace, self.o_lat, self.lse, stream)
         if self.fused:
-            L.mla_combine_out_proj(p, self.workspace, G, self.o_lat, w_uv, self.out, self.lse, stream)
+            L.mla_combine_out_proj(p, self.workspace, G, seq_lens, self.o_lat, w_uv, self.out, self.lse, stream)
         else:
             L.mla_split_kv_combine(p, self.workspace, G, self.o_lat, self.lse, stream)
             L.mla_out_proj(p, self.o_lat, w_uv, self.out, stream)

@@ -98,10 +98,11 @@ def test_host_argument_checks_return_before_any_launch():
                                 1 << 30, fake, None, None) == L.MLA_ERR_INVALID_ARG
     assert L.lib.mla_split_kv_combine(ctypes.byref(p), fake, 1 << 30, 4, odd, None, None) == L.MLA_ERR_INVALID_ARG
     f = L.lib.mla_combine_out_proj
-    assert f(ctypes.byref(p), fake, 1 << 30, 4, odd, None, fake, fake, None) == L.MLA_ERR_INVALID_ARG
-    assert f(ctypes.byref(p), fake, 1 << 30, 4, fake, None, None, fake, None) == L.MLA_ERR_INVALID_ARG
-    assert f(ctypes.byref(p), fake, 16, 4, fake, None, fake, fake, None) == L.MLA_ERR_WORKSPACE
-    assert f(ctypes.byref(p), None, 1 << 30, 4, fake, None, fake, fake, None) == L.MLA_ERR_WORKSPACE
+    assert f(ctypes.byref(p), fake, 1 << 30, 4, fake, odd, None, fake, fake, None) == L.MLA_ERR_INVALID_ARG
+    assert f(ctypes.byref(p), fake, 1 << 30, 4, fake, fake, None, None, fake, None) == L.MLA_ERR_INVALID_ARG
+    assert f(ctypes.byref(p), fake, 1 << 30, 4, None, fake, None, fake, fake, None) == L.MLA_ERR_INVALID_ARG
+    assert f(ctypes.byref(p), fake, 16, 4, fake, fake, None, fake, fake, None) == L.MLA_ERR_WORKSPACE
+    assert f(ctypes.byref(p), None, 1 << 30, 4, fake, fake, None, fake, fake, None) == L.MLA_ERR_WORKSPACE
     bad = L.make_params(B=2, H=128, max_pages_per_seq=4, num_pages=8)
     bad.kv_lora_rank = 256
     assert _call_decode(bad) == L.MLA_ERR_UNSUPPORTED

@@ -327,7 +327,7 @@ def test_combine_fused_into_out_projection(lens, G, H):
     out_b = torch.full((B, H, 128), float("nan"), dtype=torch.float32, device="cuda")
     L.mla_split_kv_combine(p, ws, G, o_a, lse_a)
     L.mla_out_proj(p, o_a, wuv, out_a)
-    L.mla_combine_out_proj(p, ws, G, o_b, wuv, out_b, lse_b)
+    L.mla_combine_out_proj(p, ws, G, i32_dev(inp["seq_lens"]), o_b, wuv, out_b, lse_b)
     torch.cuda.synchronize()
     assert L.mla_workspace_status(ws) == 0
     sms = torch.cuda.get_device_properties(0).multi_processor_count
