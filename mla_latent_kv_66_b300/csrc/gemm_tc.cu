@@ -5,11 +5,12 @@
 //
 // Both are the key and value halves of kv_b_proj (mtrt.cn DeepSeek-Coder-V2
 // MLA page, section "源码里的压缩全流程", KV decompression) applied on the
-// query and output side.  Each CTA computes one head's [128 x N] tile, N =
-// the batch rounded up to 16, with the batch as the MMA's N dimension; the
-// weights stream once through a TMA pipeline into 128-byte-swizzled shared
-// memory, the accumulator lives in tensor memory.  W_UK is read with its
-// latent axis as M, i.e. as an MN-major A operand; W_UV is K-major.
+// query and output side.  The batch (rounded up to 16) is the MMA's N
+// dimension, the weights stream once by TMA into 128-byte-swizzled shared
+// memory and the accumulators live in tensor memory.  The absorption takes
+// one CTA per head (its four 128-row M tiles of W_UK, read with the latent
+// axis as M, i.e. as an MN-major A operand); the out-projection one CTA per
+// head's [128 x N] tile (W_UV K-major).
 #include <algorithm>
 
 #include "combine.cuh"
@@ -26,19 +27,18 @@ constexpr uint32_t kABytes = 16384;  // A bytes per 64-wide K block
 
 struct GemmTcArgs {
   int B, H, N;
-  int S;                        // pipeline stages (K blocks in flight), at most kMaxS
+  int S;                        // out-projection: pipeline stages (K blocks in flight), at most kMaxS
   const __nv_bfloat16* weight;  // [H,128,512]: prefetched into L2 before the dependency wait
   void* out;
-  int out_kind;  // 0: q_lat bf16 [B,H,512]; 1: out fp32 [B,H,128]; 2: out bf16 [B,H,128]
+  int out_kind;  // absorption: q_lat bf16 [B,H,512] (unused); out-projection: 1 fp32, 2 bf16 [B,H,128]
 };
 
 constexpr int kMaxS = 8;
 
-template <int kMode>
 __global__ void __launch_bounds__(128, 1)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__ CUtensorMap tB,
-                   GemmTcArgs g) {
-  constexpr int KB = kMode == 0 ? 2 : 8;  // K blocks of 64
+    outproj_tc_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__ CUtensorMap tB,
+                      GemmTcArgs g) {
+  constexpr int KB = 8;  // K blocks of 64
   const int S = g.S;                      // pipeline stages
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bars[2 * kMaxS + 1];
@@ -49,16 +49,13 @@ __global__ void __launch_bounds__(128, 1)
   const uint32_t b_bytes = (uint32_t)g.N * 128u;
   const uint32_t stage = kABytes + b_bytes;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = blockIdx.x, mt = blockIdx.y, nt = blockIdx.z;
+  const int h = blockIdx.x, nt = blockIdx.z;
   const uint32_t full = smem_u32(&bars[0]), empty = smem_u32(&bars[kMaxS]), done = smem_u32(&bars[2 * kMaxS]);
   const uint32_t ncols = g.N <= 32 ? 32 : g.N <= 64 ? 64 : g.N <= 128 ? 128 : 256;
 
-  // q absorption opens a decode step: the decode kernel may launch at once.
-  // The out-projection follows the combine: its weight slice (independent of
-  // the combine) is pulled into L2 while the combine runs.
-  if (kMode == 0) grid_dep_trigger();
-  if (kMode == 1 && threadIdx.x == 32 && mt == 0 && nt == 0)
-    prefetch_l2(g.weight + (size_t)h * kV * kLatent, kV * kLatent * 2);
+  // the out-projection follows the combine: its weight slice (independent of
+  // the combine) is pulled into L2 while the combine runs
+  if (threadIdx.x == 32 && nt == 0) prefetch_l2(g.weight + (size_t)h * kV * kLatent, kV * kLatent * 2);
   grid_dep_wait();
   if (threadIdx.x == 0) {
     abort_flag = 0;
@@ -88,12 +85,7 @@ __global__ void __launch_bounds__(128, 1)
       if (kb >= S && !mbar_wait(empty + 8 * s, ((kb / S) - 1) & 1, &abort_flag, nullptr)) break;
       const uint32_t a_s = base + s * stage, b_s = a_s + kABytes;
       mbar_expect_tx(full + 8 * s, stage);
-      if (kMode == 0) {
-        tma_load_2d(a_s, &tA, full + 8 * s, mt * 128, h * 128 + kb * 64);
-        tma_load_2d(a_s + 8192, &tA, full + 8 * s, mt * 128 + 64, h * 128 + kb * 64);
-      } else {
-        tma_load_2d(a_s, &tA, full + 8 * s, kb * 64, h * 128);
-      }
+      tma_load_2d(a_s, &tA, full + 8 * s, kb * 64, h * 128);
       tma_load_3d(b_s, &tB, full + 8 * s, kb * 64, h, nt * g.N);
       ++issued;
     }
@@ -105,7 +97,7 @@ __global__ void __launch_bounds__(128, 1)
     }
   } else if (warp == 1 && lane == 0) {
     // MMA issuer
-    const uint32_t idesc = idesc_bf16(128, g.N, kMode == 0, false);
+    const uint32_t idesc = idesc_bf16(128, g.N, false, false);
     for (int kb = 0; kb < KB; ++kb) {
       const int s = kb % S;
       if (!mbar_wait(full + 8 * s, (kb / S) & 1, &abort_flag, nullptr)) break;
@@ -113,9 +105,8 @@ __global__ void __launch_bounds__(128, 1)
       const uint32_t a_s = base + s * stage, b_s = a_s + kABytes;
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        // MN-major A advances 16 K-rows (2 KB); K-major operands advance 32 B
-        const uint64_t ad = kMode == 0 ? sdesc_sw128(a_s + k * 2048, 8192, 1024)
-                                       : sdesc_sw128(a_s + k * 32, 16, 1024);
+        // K-major operands advance 32 B per 16-wide K step
+        const uint64_t ad = sdesc_sw128(a_s + k * 32, 16, 1024);
         const uint64_t bd = sdesc_sw128(b_s + k * 32, 16, 1024);
         mma_bf16_ss(tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
       }
@@ -139,9 +130,7 @@ __global__ void __launch_bounds__(128, 1)
       if (b >= g.B) break;
       const float v = ok ? __uint_as_float(r[j]) : __int_as_float(0x7fc00000);
       const size_t bh = (size_t)b * g.H + h;
-      if (g.out_kind == 0)
-        static_cast<__nv_bfloat16*>(g.out)[bh * kLatent + mt * 128 + row] = __float2bfloat16_rn(v);
-      else if (g.out_kind == 1)
+      if (g.out_kind == 1)
         static_cast<float*>(g.out)[bh * kV + row] = v;
       else
         static_cast<__nv_bfloat16*>(g.out)[bh * kV + row] = __float2bfloat16_rn(v);
@@ -152,6 +141,117 @@ __global__ void __launch_bounds__(128, 1)
   if (warp == 2) {
     tc_fence_after();
     tmem_dealloc(tmem, ncols);
+  }
+}
+
+// ---------------------------------------------------------------- q absorption
+// One 512-thread CTA per (head, batch tile): the head's whole W_UK slice
+// (128 x 512 bf16, 128 KB) goes out by TMA at once, one barrier per 128-row
+// M tile, followed by the q_nope rows; the four tiles accumulate in four
+// tensor-memory accumulators, and warp w writes tile w / 4 from the lanes of
+// its sub-partition.  Compared with one CTA per (head, M tile), q_nope is
+// read once per head and a quarter as many CTAs are launched.
+constexpr int kAbsorbThreads = 512;
+constexpr int kAbsorbMaxN = 128;  // four accumulators of N columns fill the 512
+
+__global__ void __launch_bounds__(kAbsorbThreads, 1)
+    absorb_tc_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__ CUtensorMap tB,
+                     GemmTcArgs g) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bars[9];  // [0,4) W_UK tile mt landed, 4 q_nope landed, [5,9) tile mt done
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t b_blk = (uint32_t)g.N * 128u;    // one 64-wide K block of q_nope
+  const uint32_t bbase = base + 8u * kABytes;     // A: 4 tiles x 2 K blocks
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.x, nt = blockIdx.z;
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+  const uint32_t acols = g.N <= 32 ? 32 : g.N <= 64 ? 64 : 128;
+
+  // q absorption opens a decode step: the decode kernel may launch at once
+  grid_dep_trigger();
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int i = 0; i < 9; ++i) mbar_init(bar(i), 1);
+    fence_mbar_init();
+    prefetch_tmap(&tA);
+    prefetch_tmap(&tB);
+    // W_UK does not depend on the preceding kernel: all of it goes out now
+    for (int mt = 0; mt < 4; ++mt) {
+      mbar_expect_tx(bar(mt), 2 * kABytes);
+      for (int kb = 0; kb < 2; ++kb) {
+        const uint32_t a_s = base + (uint32_t)(mt * 2 + kb) * kABytes;
+        tma_load_2d(a_s, &tA, bar(mt), mt * 128, h * 128 + kb * 64);
+        tma_load_2d(a_s + 8192, &tA, bar(mt), mt * 128 + 64, h * 128 + kb * 64);
+      }
+    }
+  }
+  if (warp == 2) {
+    tmem_alloc(smem_u32(&tmem_slot), 4 * acols);
+    tmem_relinquish();
+  }
+  grid_dep_wait();  // q_nope may be written by the preceding kernel
+  if (threadIdx.x == 0) {
+    mbar_expect_tx(bar(4), 2 * b_blk);
+    for (int kb = 0; kb < 2; ++kb) tma_load_3d(bbase + kb * b_blk, &tB, bar(4), kb * 64, h, nt * g.N);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  if (warp == 1 && lane == 0) {
+    // MMA issuer: each tile as soon as its W_UK slice has landed; A is the
+    // MN-major weight (16 K-rows = 2 KB per MMA), B the K-major q_nope rows
+    const uint32_t idesc = idesc_bf16(128, g.N, true, false);
+    bool ok = mbar_wait(bar(4), 0, &abort_flag, nullptr);
+    for (int mt = 0; ok && mt < 4; ++mt) {
+      if (!mbar_wait(bar(mt), 0, &abort_flag, nullptr)) break;
+      tc_fence_after();
+#pragma unroll
+      for (int kb = 0; kb < 2; ++kb) {
+        const uint32_t a_s = base + (uint32_t)(mt * 2 + kb) * kABytes, b_s = bbase + kb * b_blk;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma_bf16_ss(tmem + mt * acols, sdesc_sw128(a_s + k * 2048, 8192, 1024),
+                      sdesc_sw128(b_s + k * 32, 16, 1024), idesc, (kb | k) != 0 ? 1u : 0u);
+      }
+      mma_commit(bar(5 + mt));
+    }
+  }
+  __syncwarp();
+
+  // epilogue: warp w writes tile mt = w / 4 (latent columns [128 mt, 128 mt
+  // + 128)), thread = latent column, columns of the accumulator = batch
+  const int mt = warp >> 2, q = warp & 3;
+  const bool ok = mbar_wait(bar(5 + mt), 0, &abort_flag, nullptr) && !abort_flag;
+  tc_fence_after();
+  const int col = mt * 128 + q * 32 + lane;
+  for (int c0 = 0; c0 < g.N; c0 += 16) {
+    uint32_t r[16];
+    tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(mt * acols + c0), r);
+    tmem_wait_ld();
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int b = nt * g.N + c0 + j;
+      if (b >= g.B) break;
+      const float v = ok ? __uint_as_float(r[j]) : __int_as_float(0x7fc00000);
+      static_cast<__nv_bfloat16*>(g.out)[((size_t)b * g.H + h) * kLatent + col] = __float2bfloat16_rn(v);
+    }
+  }
+  if (abort_flag && threadIdx.x == 0) {  // copies in flight land before the CTA exits
+    for (int i = 0; i < 5; ++i) {
+      volatile int no_abort = 0;
+      mbar_wait(bar(i), 0, &no_abort, nullptr);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 4 * acols);
   }
 }
 
@@ -392,7 +492,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 cudaError_t launch_absorb_tc(const __nv_bfloat16* q_nope, const __nv_bfloat16* w_uk,
                              __nv_bfloat16* q_lat, int B, int H, cudaStream_t stream) {
   if (!aligned16(q_nope) || !aligned16(w_uk)) return cudaErrorInvalidValue;
-  const int N = batch_tile(B);
+  const int N = std::min(batch_tile(B), kAbsorbMaxN);
   CUtensorMap tA, tB;
   const cuuint64_t ad[2] = {kLatent, (cuuint64_t)H * kNope}, as[1] = {kLatent * 2};
   const cuuint32_t abox[2] = {64, 64};
@@ -402,12 +502,12 @@ cudaError_t launch_absorb_tc(const __nv_bfloat16* q_nope, const __nv_bfloat16* w
   if (!make_tmap(&tA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w_uk, ad, as, abox) ||
       !make_tmap(&tB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q_nope, bd, bs, bbox))
     return cudaErrorInvalidValue;
-  GemmTcArgs g{B, H, N, 2, w_uk, q_lat, 0};
-  const size_t smem = 2 * (kABytes + (size_t)N * 128) + 1024;
-  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  GemmTcArgs g{B, H, N, 0, w_uk, q_lat, 0};
+  const size_t smem = 8 * kABytes + 2 * (size_t)N * 128 + 1024;
+  cudaError_t e = cudaFuncSetAttribute(absorb_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(H, kLatent / 128, (B + N - 1) / N);
-  gemm_tc_kernel<0><<<grid, 128, smem, stream>>>(tA, tB, g);
+  dim3 grid(H, 1, (B + N - 1) / N);
+  absorb_tc_kernel<<<grid, kAbsorbThreads, smem, stream>>>(tA, tB, g);
   return cudaGetLastError();
 }
 
@@ -430,10 +530,10 @@ cudaError_t launch_out_proj_tc(const __nv_bfloat16* o_lat, const __nv_bfloat16* 
   const int S = (int)std::min<size_t>(kMaxS, (200u << 10) / stage);
   GemmTcArgs g{B, H, N, S, w_uv, out, out_bf16 ? 2 : 1};
   const size_t smem = S * stage + 1024;
-  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(outproj_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(H, 1, (B + N - 1) / N);
-  return launch_dependent(gemm_tc_kernel<1>, grid, dim3(128), smem, stream, tA, tB, g);
+  return launch_dependent(outproj_tc_kernel, grid, dim3(128), smem, stream, tA, tB, g);
 }
 
 cudaError_t launch_outproj_combine(const __nv_bfloat16* part_o, const float* part_lse, const int32_t* seq_lens,
