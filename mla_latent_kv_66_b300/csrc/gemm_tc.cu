@@ -145,28 +145,33 @@ __global__ void __launch_bounds__(128, 1)
 }
 
 // ---------------------------------------------------------------- q absorption
-// One 512-thread CTA per (head, batch tile): the head's whole W_UK slice
-// (128 x 512 bf16, 128 KB) goes out by TMA at once, one barrier per 128-row
-// M tile, followed by the q_nope rows; the four tiles accumulate in four
-// tensor-memory accumulators, and warp w writes tile w / 4 from the lanes of
-// its sub-partition.  Compared with one CTA per (head, M tile), q_nope is
-// read once per head and a quarter as many CTAs are launched.
-constexpr int kAbsorbThreads = 512;
+// One CTA of 128 kAbsorbTiles threads per (head, group of kAbsorbTiles
+// 128-row M tiles of W_UK^T, batch tile): the group's W_UK slice (32 KB per
+// tile) goes out by TMA at once, one barrier per tile, followed by the
+// q_nope rows; each tile accumulates in its own tensor-memory accumulator,
+// and warp w writes tile w / 4 from the lanes of its sub-partition.  With
+// all four tiles in one CTA, q_nope is read once per head and a quarter as
+// many CTAs are launched as with one tile per CTA.
+constexpr int kAbsorbTiles = 4;
 constexpr int kAbsorbMaxN = 128;  // four accumulators of N columns fill the 512
 
-__global__ void __launch_bounds__(kAbsorbThreads, 1)
+template <int kTiles>
+__global__ void __launch_bounds__(128 * kTiles, 1)
     absorb_tc_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__ CUtensorMap tB,
                      GemmTcArgs g) {
+  static_assert(kTiles == 1 || kTiles == 2 || kTiles == 4, "tiles per CTA");
+  constexpr int kQ = kTiles;          // barrier: q_nope landed
+  constexpr int kDone = kTiles + 1;   // barriers: tile lt done
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bars[9];  // [0,4) W_UK tile mt landed, 4 q_nope landed, [5,9) tile mt done
+  __shared__ __align__(8) uint64_t bars[2 * kTiles + 1];  // [0, kTiles) W_UK tile lt landed
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  const uint32_t b_blk = (uint32_t)g.N * 128u;    // one 64-wide K block of q_nope
-  const uint32_t bbase = base + 8u * kABytes;     // A: 4 tiles x 2 K blocks
+  const uint32_t b_blk = (uint32_t)g.N * 128u;               // one 64-wide K block of q_nope
+  const uint32_t bbase = base + 2u * kTiles * kABytes;       // A: kTiles tiles x 2 K blocks
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = blockIdx.x, nt = blockIdx.z;
+  const int h = blockIdx.x, mt0 = blockIdx.y * kTiles, nt = blockIdx.z;
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
   const uint32_t acols = g.N <= 32 ? 32 : g.N <= 64 ? 64 : 128;
 
@@ -174,28 +179,29 @@ __global__ void __launch_bounds__(kAbsorbThreads, 1)
   grid_dep_trigger();
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    for (int i = 0; i < 9; ++i) mbar_init(bar(i), 1);
+    for (int i = 0; i < 2 * kTiles + 1; ++i) mbar_init(bar(i), 1);
     fence_mbar_init();
     prefetch_tmap(&tA);
     prefetch_tmap(&tB);
     // W_UK does not depend on the preceding kernel: all of it goes out now
-    for (int mt = 0; mt < 4; ++mt) {
-      mbar_expect_tx(bar(mt), 2 * kABytes);
+    for (int lt = 0; lt < kTiles; ++lt) {
+      const int mt = mt0 + lt;
+      mbar_expect_tx(bar(lt), 2 * kABytes);
       for (int kb = 0; kb < 2; ++kb) {
-        const uint32_t a_s = base + (uint32_t)(mt * 2 + kb) * kABytes;
-        tma_load_2d(a_s, &tA, bar(mt), mt * 128, h * 128 + kb * 64);
-        tma_load_2d(a_s + 8192, &tA, bar(mt), mt * 128 + 64, h * 128 + kb * 64);
+        const uint32_t a_s = base + (uint32_t)(lt * 2 + kb) * kABytes;
+        tma_load_2d(a_s, &tA, bar(lt), mt * 128, h * 128 + kb * 64);
+        tma_load_2d(a_s + 8192, &tA, bar(lt), mt * 128 + 64, h * 128 + kb * 64);
       }
     }
   }
   if (warp == 2) {
-    tmem_alloc(smem_u32(&tmem_slot), 4 * acols);
+    tmem_alloc(smem_u32(&tmem_slot), kTiles * acols);
     tmem_relinquish();
   }
   grid_dep_wait();  // q_nope may be written by the preceding kernel
   if (threadIdx.x == 0) {
-    mbar_expect_tx(bar(4), 2 * b_blk);
-    for (int kb = 0; kb < 2; ++kb) tma_load_3d(bbase + kb * b_blk, &tB, bar(4), kb * 64, h, nt * g.N);
+    mbar_expect_tx(bar(kQ), 2 * b_blk);
+    for (int kb = 0; kb < 2; ++kb) tma_load_3d(bbase + kb * b_blk, &tB, bar(kQ), kb * 64, h, nt * g.N);
   }
   tc_fence_before();
   __syncthreads();
@@ -206,32 +212,32 @@ __global__ void __launch_bounds__(kAbsorbThreads, 1)
     // MMA issuer: each tile as soon as its W_UK slice has landed; A is the
     // MN-major weight (16 K-rows = 2 KB per MMA), B the K-major q_nope rows
     const uint32_t idesc = idesc_bf16(128, g.N, true, false);
-    bool ok = mbar_wait(bar(4), 0, &abort_flag, nullptr);
-    for (int mt = 0; ok && mt < 4; ++mt) {
-      if (!mbar_wait(bar(mt), 0, &abort_flag, nullptr)) break;
+    bool ok = mbar_wait(bar(kQ), 0, &abort_flag, nullptr);
+    for (int lt = 0; ok && lt < kTiles; ++lt) {
+      if (!mbar_wait(bar(lt), 0, &abort_flag, nullptr)) break;
       tc_fence_after();
 #pragma unroll
       for (int kb = 0; kb < 2; ++kb) {
-        const uint32_t a_s = base + (uint32_t)(mt * 2 + kb) * kABytes, b_s = bbase + kb * b_blk;
+        const uint32_t a_s = base + (uint32_t)(lt * 2 + kb) * kABytes, b_s = bbase + kb * b_blk;
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          mma_bf16_ss(tmem + mt * acols, sdesc_sw128(a_s + k * 2048, 8192, 1024),
+          mma_bf16_ss(tmem + lt * acols, sdesc_sw128(a_s + k * 2048, 8192, 1024),
                       sdesc_sw128(b_s + k * 32, 16, 1024), idesc, (kb | k) != 0 ? 1u : 0u);
       }
-      mma_commit(bar(5 + mt));
+      mma_commit(bar(kDone + lt));
     }
   }
   __syncwarp();
 
-  // epilogue: warp w writes tile mt = w / 4 (latent columns [128 mt, 128 mt
+  // epilogue: warp w writes tile lt = w / 4 (latent columns [128 mt, 128 mt
   // + 128)), thread = latent column, columns of the accumulator = batch
-  const int mt = warp >> 2, q = warp & 3;
-  const bool ok = mbar_wait(bar(5 + mt), 0, &abort_flag, nullptr) && !abort_flag;
+  const int lt = warp >> 2, q = warp & 3;
+  const bool ok = mbar_wait(bar(kDone + lt), 0, &abort_flag, nullptr) && !abort_flag;
   tc_fence_after();
-  const int col = mt * 128 + q * 32 + lane;
+  const int col = (mt0 + lt) * 128 + q * 32 + lane;
   for (int c0 = 0; c0 < g.N; c0 += 16) {
     uint32_t r[16];
-    tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(mt * acols + c0), r);
+    tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(lt * acols + c0), r);
     tmem_wait_ld();
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
@@ -242,7 +248,7 @@ __global__ void __launch_bounds__(kAbsorbThreads, 1)
     }
   }
   if (abort_flag && threadIdx.x == 0) {  // copies in flight land before the CTA exits
-    for (int i = 0; i < 5; ++i) {
+    for (int i = 0; i <= kQ; ++i) {
       volatile int no_abort = 0;
       mbar_wait(bar(i), 0, &no_abort, nullptr);
     }
@@ -251,7 +257,7 @@ __global__ void __launch_bounds__(kAbsorbThreads, 1)
   __syncthreads();
   if (warp == 2) {
     tc_fence_after();
-    tmem_dealloc(tmem, 4 * acols);
+    tmem_dealloc(tmem, kTiles * acols);
   }
 }
 
@@ -503,11 +509,12 @@ cudaError_t launch_absorb_tc(const __nv_bfloat16* q_nope, const __nv_bfloat16* w
       !make_tmap(&tB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q_nope, bd, bs, bbox))
     return cudaErrorInvalidValue;
   GemmTcArgs g{B, H, N, 0, w_uk, q_lat, 0};
-  const size_t smem = 8 * kABytes + 2 * (size_t)N * 128 + 1024;
-  cudaError_t e = cudaFuncSetAttribute(absorb_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const size_t smem = 2 * kAbsorbTiles * kABytes + 2 * (size_t)N * 128 + 1024;
+  auto kernel = absorb_tc_kernel<kAbsorbTiles>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(H, 1, (B + N - 1) / N);
-  absorb_tc_kernel<<<grid, kAbsorbThreads, smem, stream>>>(tA, tB, g);
+  dim3 grid(H, 4 / kAbsorbTiles, (B + N - 1) / N);
+  kernel<<<grid, 128 * kAbsorbTiles, smem, stream>>>(tA, tB, g);
   return cudaGetLastError();
 }
 
