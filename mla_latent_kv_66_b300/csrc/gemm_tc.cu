@@ -448,19 +448,22 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   }
   __syncwarp();
 
-  // epilogue (warps 0-3, one per 32 tensor-memory lanes): thread = v row,
-  // columns = batch; the other warps go straight to the closing barrier
-  // (fewer threads polling the barrier while the MMAs read shared memory)
-  if (warp < 4) {
+  // epilogue: warp w reads the tensor-memory lanes of its sub-partition
+  // (w % 4: 32 v rows, thread = v row) and batch columns [8 (w / 4), +8) of
+  // every 32, so all 16 warps share the stores
+  {
     const bool ok = mbar_wait(done, 0, &abort_flag, nullptr) && !abort_flag;
     tc_fence_after();
-    const int row = warp * 32 + lane;
-    for (int c0 = 0; c0 < g.N; c0 += 16) {
-      uint32_t r[16];
-      tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, r);
+    const int q = warp & 3, row = q * 32 + lane;
+    for (int c0 = (warp >> 2) * 8; c0 < g.N; c0 += 32) {
+      uint32_t r[8];
+      asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                   : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                   : "r"(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0)
+                   : "memory");
       tmem_wait_ld();
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
+      for (int j = 0; j < 8; ++j) {
         const int b = nt * g.N + c0 + j;
         if (b >= g.B) break;
         const float v = ok ? __uint_as_float(r[j]) : __int_as_float(0x7fc00000);
