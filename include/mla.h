@@ -20,8 +20,9 @@
  * Conventions for every call:
  *  - All tensors are dense, row-major, contiguous, in device memory unless
  *    a comment says "host".  The caller owns every buffer and the stream.
- *    mla_decode and mla_split_kv_combine want every tensor and the
- *    workspace 16-byte aligned (MLA_ERR_INVALID_ARG otherwise).
+ *    mla_absorb_q, mla_decode, mla_split_kv_combine and mla_combine_out_proj
+ *    want every tensor and the workspace 16-byte aligned
+ *    (MLA_ERR_INVALID_ARG otherwise).
  *  - No call allocates memory or synchronises, except mla_workspace_status
  *    and mla_decode_static_status, which read one word back.  Calls only
  *    enqueue work on `stream`.

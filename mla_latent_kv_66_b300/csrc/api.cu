@@ -134,6 +134,7 @@ mla_status mla_absorb_q(const mla_params* p, const void* q_nope, const void* w_u
   mla_status s = check_params(p);
   if (s != MLA_OK) return s;
   if (!q_nope || !w_uk || !q_lat) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q_nope) || !aligned16(w_uk) || !aligned16(q_lat)) return MLA_ERR_INVALID_ARG;
   return cuda_status(launch_absorb_tc(static_cast<const __nv_bfloat16*>(q_nope),
                                         static_cast<const __nv_bfloat16*>(w_uk),
                                         static_cast<__nv_bfloat16*>(q_lat), p->B, p->H,

@@ -230,22 +230,37 @@ __global__ void __launch_bounds__(128 * kTiles, 1)
   __syncwarp();
 
   // epilogue: warp w writes tile lt = w / 4 (latent columns [128 mt, 128 mt
-  // + 128)), thread = latent column, columns of the accumulator = batch
+  // + 128)); thread = latent column, columns of the accumulator = batch.  The
+  // warp's [N x 32] bf16 block is staged in the tile's own W_UK buffer (its
+  // MMAs are done) and leaves in 16-byte stores along the latent axis.
   const int lt = warp >> 2, q = warp & 3;
   const bool ok = mbar_wait(bar(kDone + lt), 0, &abort_flag, nullptr) && !abort_flag;
   tc_fence_after();
-  const int col = (mt0 + lt) * 128 + q * 32 + lane;
+  const uint32_t stg = base + (uint32_t)lt * 2u * kABytes + (uint32_t)q * 8192u;  // N x 64 B <= 8 KB
   for (int c0 = 0; c0 < g.N; c0 += 16) {
     uint32_t r[16];
     tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(lt * acols + c0), r);
     tmem_wait_ld();
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
-      const int b = nt * g.N + c0 + j;
-      if (b >= g.B) break;
       const float v = ok ? __uint_as_float(r[j]) : __int_as_float(0x7fc00000);
-      static_cast<__nv_bfloat16*>(g.out)[((size_t)b * g.H + h) * kLatent + col] = __float2bfloat16_rn(v);
+      const __nv_bfloat16 hv = __float2bfloat16_rn(v);
+      asm volatile("st.shared.b16 [%0], %1;" ::"r"(stg + (uint32_t)((c0 + j) * 32 + lane) * 2u),
+                   "h"(*reinterpret_cast<const uint16_t*>(&hv))
+                   : "memory");
     }
+  }
+  __syncwarp();
+  const int col0 = (mt0 + lt) * 128 + q * 32;
+  for (int k = lane; k < g.N * 4; k += 32) {  // 16-byte chunk p of batch row bl
+    const int bl = k >> 2, p = k & 3, b = nt * g.N + bl;
+    if (b >= g.B) break;
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(stg + (uint32_t)(bl * 64 + p * 16))
+                 : "memory");
+    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(g.out) + ((size_t)b * g.H + h) * kLatent + col0 + p * 8) = v;
   }
   if (abort_flag && threadIdx.x == 0) {  // copies in flight land before the CTA exits
     for (int i = 0; i <= kQ; ++i) {
@@ -500,7 +515,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 cudaError_t launch_absorb_tc(const __nv_bfloat16* q_nope, const __nv_bfloat16* w_uk,
                              __nv_bfloat16* q_lat, int B, int H, cudaStream_t stream) {
-  if (!aligned16(q_nope) || !aligned16(w_uk)) return cudaErrorInvalidValue;
+  if (!aligned16(q_nope) || !aligned16(w_uk) || !aligned16(q_lat)) return cudaErrorInvalidValue;
   const int N = std::min(batch_tile(B), kAbsorbMaxN);
   CUtensorMap tA, tB;
   const cuuint64_t ad[2] = {kLatent, (cuuint64_t)H * kNope}, as[1] = {kLatent * 2};

@@ -114,6 +114,11 @@ def test_host_argument_checks_return_before_any_launch():
     assert _call_decode(bad) == L.MLA_ERR_INVALID_ARG
     fake = ctypes.c_void_p(0x1000)
     assert L.lib.mla_absorb_q(ctypes.byref(p), None, fake, fake, None) == L.MLA_ERR_INVALID_ARG
+    odd8 = ctypes.c_void_p(0x1008)
+    for i in range(3):  # q_nope, w_uk, q_lat: 16-byte alignment
+        args = [fake] * 3
+        args[i] = odd8
+        assert L.lib.mla_absorb_q(ctypes.byref(p), *args, None) == L.MLA_ERR_INVALID_ARG
     assert L.lib.mla_out_proj(ctypes.byref(p), fake, None, fake, None) == L.MLA_ERR_INVALID_ARG
     assert L.lib.mla_cache_append(ctypes.byref(p), fake, fake, fake, -1, 3, fake, fake, None, None) \
         == L.MLA_ERR_INVALID_ARG
