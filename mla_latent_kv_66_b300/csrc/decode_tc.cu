@@ -133,6 +133,7 @@ enum {
   B_OFREE,
   B_QFULL,
   B_IDLE,
+  B_QTMA,                           // bf16: the first unit's query landed (TMA)
   B_COUNT
 };
 
@@ -365,8 +366,9 @@ __device__ inline float load_q8_rows(const DecodeArgs& a, uint32_t tq, uint32_t 
 
 template <int kMode>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    decode_tc_kernel(const __grid_constant__ CUtensorMap tm_ckv,
-                     const __grid_constant__ CUtensorMap tm_kpe, DecodeArgs a) {
+    decode_tc_kernel(const __grid_constant__ CUtensorMap tm_ckv, const __grid_constant__ CUtensorMap tm_kpe,
+                     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qpe,
+                     DecodeArgs a) {
   using L = Layout<kMode>;
   constexpr bool kFp8 = kMode == 1;  // E4M3 cache expanded to bf16 in shared memory
   constexpr bool kF8 = kMode == 2;   // E4M3 cache on the 8-bit tensor cores
@@ -426,10 +428,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(bar(B_OFREE), 256);
     mbar_init(bar(B_QFULL), 256);  // the softmax threads (first unit) or the exchange threads twice
     mbar_init(bar(B_IDLE), 2);
+    mbar_init(bar(B_QTMA), 1);
     for (int i = 0; i < 4; ++i) mbar_expect_tx(bar(B_XFULL + i), kSlab);
     fence_mbar_init();
     prefetch_tmap(&tm_ckv);
     prefetch_tmap(&tm_kpe);
+    if (kMode == 0) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_qpe);
+    }
   }
 
   // ---------------------------------------------------------------- producer state
@@ -926,7 +933,49 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint32_t g = 0, uc = 0;
     bool ok = true;
     bool have = wk.next(a, u);
-    if (have && !kF8) {  // the first unit's query: warpgroup j loads half j of the latent part
+    if (have && kMode == 0) {
+      // the first unit's query: this CTA's latent half by TMA into stages 1-2
+      // (free until the rest of the ring goes out, after B_QFULL; four
+      // [128 rows x 64] boxes, 128-byte swizzle) and its RoPE half straight
+      // into the operand's place (64-byte swizzle); warpgroup j then moves
+      // latent half j into tensor memory.  Rows h >= H hold other rows of
+      // q_lat or TMA zeros and are zeroed here.
+      const uint32_t qs = base + kStageBytes;
+      if (h == 0 && j == 0) {
+        mbar_expect_tx(bar(B_QTMA), 4 * 16384 + 8192);
+        for (int k = 0; k < 4; ++k)
+          tma_load_2d(qs + k * 16384, &tm_q, bar(B_QTMA), (int)rank * 256 + k * 64, u.b * H);
+        tma_load_2d(base + kOffQpe, &tm_qpe, bar(B_QTMA), (int)rank * 32, u.b * H);
+      }
+      ok = wwait(B_QTMA, 0);
+      if (!ok && h == 0 && j == 0) {  // the copies land before the CTA can exit
+        volatile int no_abort = 0;
+        mbar_wait(bar(B_QTMA), 0, &no_abort, nullptr);
+      }
+      const bool on = h < H;
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const uint32_t row = qs + (uint32_t)(2 * j + cc) * 16384u + (uint32_t)h * 128u;
+        uint32_t r[32];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 v = on ? ld_shared_v4u(row + ((uint32_t)(c ^ (h & 7)) << 4)) : make_uint4(0, 0, 0, 0);
+          r[4 * c] = v.x;
+          r[4 * c + 1] = v.y;
+          r[4 * c + 2] = v.z;
+          r[4 * c + 3] = v.w;
+        }
+        tmem_st32(tmem + lane_base + kTmQ + j * 64 + cc * 32, r);
+      }
+      if (j == 0 && !on) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) st_shared_v4(base + kOffQpe + h * 64 + c * 16, 0, 0, 0, 0);
+      }
+      tmem_wait_st();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(B_QFULL));
+    } else if (have && kFp8) {  // the first unit's query: warpgroup j loads half j of the latent part
       load_q_rows(a, tmem + lane_base + kTmQ, base + kOffQpe, u.b, h, rank, j, j + 1, j == 0);
       tmem_wait_st();
       fence_proxy_async_smem();
@@ -1211,11 +1260,20 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t stream) {
                    CU_TENSOR_MAP_SWIZZLE_64B))
       return cudaErrorInvalidValue;
   }
+  // the first unit's query (bf16 cache): [B*H rows x 512] latent, [B*H x 64] RoPE
+  CUtensorMap tq_map, tqp_map;
+  const cuuint64_t rows_q = (cuuint64_t)a.B * a.H;
+  const cuuint64_t qd[2] = {kLatent, rows_q}, qst[1] = {kLatent * 2}, pd[2] = {kRope, rows_q}, pst[1] = {kRope * 2};
+  const cuuint32_t qbox[2] = {64, 128}, pbox[2] = {32, 128};
+  if ((reinterpret_cast<uintptr_t>(a.q_lat) & 15) || (reinterpret_cast<uintptr_t>(a.q_pe) & 15) ||
+      !make_tmap(&tq_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.q_lat, qd, qst, qbox) ||
+      !make_tmap(&tqp_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.q_pe, pd, pst, pbox, CU_TENSOR_MAP_SWIZZLE_64B))
+    return cudaErrorInvalidValue;
   auto kernel = mma8 ? decode_tc_kernel<2> : fp8 ? decode_tc_kernel<1> : decode_tc_kernel<0>;
   const uint32_t smem = mma8 ? Layout<2>::kSmemBytes : fp8 ? Layout<1>::kSmemBytes : Layout<0>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  return launch_dependent(kernel, dim3(2 * a.G), dim3(kThreads), smem, stream, tc_map, tk_map, a);
+  return launch_dependent(kernel, dim3(2 * a.G), dim3(kThreads), smem, stream, tc_map, tk_map, tq_map, tqp_map, a);
 }
 
 }  // namespace mla
