@@ -279,6 +279,23 @@ __device__ inline float ld_shared_f32(uint32_t addr) {
   asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
   return v;
 }
+// TMA tile load with an L2 cache policy: the cache pages are read once per
+// step, so they are loaded evict-first and leave the L2 to what is read
+// again (the partials the combine merges, the query, the weights).
+__device__ inline uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ inline void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
+                                        uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "l"(pol)
+      : "memory");
+}
+
 __device__ inline float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -461,6 +478,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     ++id_count;
   };
   auto issue = [&](uint32_t g) {
+    const uint64_t l2_once = l2_evict_first_policy();
     const uint32_t s = g % kRing;
     int page = page_at(g);
     if (page < 0) page = 0;  // a bad page id: masked by the softmax warps
@@ -470,9 +488,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t fb = bar(kF8 ? B_FULL + s : B_RFULL + s);
       const uint32_t dst = kF8 ? base + s * kStageBytes : base + L::kOffRaw + s * kRawBytes;
       mbar_expect_tx(fb, 2 * 8192 + 2048 + kPage * 4);
-      tma_load_2d(dst, &tm_ckv, fb, (int)rank * 256, page * kPage);
-      tma_load_2d(dst + 8192, &tm_ckv, fb, (int)rank * 256 + 128, page * kPage);
-      tma_load_2d(dst + kRawKpe, &tm_kpe, fb, (int)rank * 32, page * kPage);
+      tma_load_2d_hint(dst, &tm_ckv, fb, (int)rank * 256, page * kPage, l2_once);
+      tma_load_2d_hint(dst + 8192, &tm_ckv, fb, (int)rank * 256 + 128, page * kPage, l2_once);
+      tma_load_2d_hint(dst + kRawKpe, &tm_kpe, fb, (int)rank * 32, page * kPage, l2_once);
       bulk_copy_g2s(dst + kRawScale, a.kv_scale + (size_t)page * kPage, kPage * 4, fb);
     } else {
       const uint32_t fb = bar(B_FULL + s);
@@ -480,8 +498,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_expect_tx(fb, 4 * kBox + kKpeBox);
 #pragma unroll
       for (int i = 0; i < 4; ++i)
-        tma_load_2d(st + i * kBox, &tm_ckv, fb, (int)rank * 256 + i * 64, page * kPage);
-      tma_load_2d(st + 4 * kBox, &tm_kpe, fb, (int)rank * 32, page * kPage);
+        tma_load_2d_hint(st + i * kBox, &tm_ckv, fb, (int)rank * 256 + i * 64, page * kPage, l2_once);
+      tma_load_2d_hint(st + 4 * kBox, &tm_kpe, fb, (int)rank * 32, page * kPage, l2_once);
     }
   };
   if (warp == 0) {
