@@ -263,7 +263,10 @@ def run_ours(args, w, rank, world):
     def one(ev=None):
         L.mla_absorb_q(p, st["q_nope"], st["w_uk"], step.q_lat)
         if ev:
-            torch.cuda._sleep(100000)  # the decode launch is queued before the event fires
+            # the decode launch (host side: four tensor-map encodings and the
+            # launch) is queued before the event fires: a GPU spin of about
+            # 0.5 ms covers it on slow hosts too
+            torch.cuda._sleep(1_000_000)
             ev[0].record()
         L.mla_decode(p, step.q_lat, st["q_pe"], st["ckv"], st["kpe"], st["sc"], st["rows_table"], st["rows_lens"],
                      G, step.workspace, step.o_lat, step.lse)
