@@ -26,9 +26,10 @@
 //
 // Warp roles (512 threads):
 //   warp 0       KV-partition schedule and the first page ids, then the TMA
-//                producer (cache pages, stage ring); one stage load is issued
-//                before the CTA-wide start-up barrier, the rest of the ring
-//                once the first unit's query is in
+//                producer (cache pages, stage ring; bf16 pages evict-first
+//                in the L2); one stage load is issued before the CTA-wide
+//                start-up barrier, the rest of the ring once the first
+//                unit's query is in
 //   warp 1       MMA issuer for S = Q K^T (A = query in tensor memory)
 //   warp 2       tensor-memory allocation
 //   warp 3       split records; then MMA issuer for O += P V (a separate
@@ -43,12 +44,14 @@
 //                S = Q K^T is done; mode 1: expand the codes; mode 2: load the
 //                first unit's query too, publish each page's token-scale
 //                logarithms and reciprocals
-//   warps 8..15  two softmax warpgroups; warpgroup j owns tokens [32j, 32j+32)
-//                of every page, thread = head row: own staged partial + the
-//                peer's, row maximum agreed with the other warpgroup, online
-//                softmax with lazy rescaling, its half of P into tensor memory
-//                (two P buffers), its half of O rescaled when needed and
-//                written at the end of a unit.
+//   warps 8..15  two softmax warpgroups (mode 0 and 1: the first unit's
+//                query into tensor memory first, mode 0 by TMA through two
+//                ring stages that are still free); warpgroup j owns tokens
+//                [32j, 32j+32) of every page, thread = head row: own staged
+//                partial + the peer's, row maximum agreed with the other
+//                warpgroup, online softmax with lazy rescaling, its half of P
+//                into tensor memory (two P buffers), its half of O rescaled
+//                when needed and written at the end of a unit.
 // Tensor memory: O [0,256), S [256,320), P double buffer [320,384) (bf16
 // pairs, or E4M3 terms), query [384,512).
 #include <cuda_fp16.h>

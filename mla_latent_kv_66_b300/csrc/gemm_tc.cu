@@ -145,7 +145,7 @@ __global__ void __launch_bounds__(128, 1)
 }
 
 // ---------------------------------------------------------------- q absorption
-// One CTA of 128 kAbsorbTiles threads per (head, group of kAbsorbTiles
+// One CTA of 128 x kAbsorbTiles threads per (head, group of kAbsorbTiles
 // 128-row M tiles of W_UK^T, batch tile): the group's W_UK slice (32 KB per
 // tile) goes out by TMA at once, one barrier per tile, followed by the
 // q_nope rows; each tile accumulates in its own tensor-memory accumulator,
