@@ -27,7 +27,7 @@
 // Warp roles (512 threads):
 //   warp 0       KV-partition schedule and the first page ids, then the TMA
 //                producer (cache pages, stage ring; bf16 pages evict-first
-//                in the L2); two stage loads are issued before the CTA-wide
+//                in the L2); one stage load is issued before the CTA-wide
 //                start-up barrier, the rest of the ring once the first
 //                unit's query is in
 //   warp 1       MMA issuer for S = Q K^T (A = query in tensor memory)
@@ -116,7 +116,7 @@ constexpr float kRescaleLog2 = 8.f;  // lazy rescale threshold: P stays <= 2^8
 // the 14 octaves below the running maximum.
 constexpr float kRescaleLog2_8 = 2.f, kPShift8 = 6.f;
 constexpr int kIdRing = 16;          // page ids read ahead by the producer
-constexpr int kPreIssue = 2;         // stage loads issued before the start-up barrier
+constexpr int kPreIssue = 1;         // stage loads issued before the start-up barrier
 
 enum {
   B_FULL = 0,                       // bf16 stage ready (TMA landed, or E4M3 expanded)
@@ -957,13 +957,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     bool ok = true;
     bool have = wk.next(a, u);
     if (have && kMode == 0) {
-      // the first unit's query: this CTA's latent half by TMA into stages 2-3
+      // the first unit's query: this CTA's latent half by TMA into stages 1-2
       // (free until the rest of the ring goes out, after B_QFULL; four
       // [128 rows x 64] boxes, 128-byte swizzle) and its RoPE half straight
       // into the operand's place (64-byte swizzle); warpgroup j then moves
       // latent half j into tensor memory.  Rows h >= H hold other rows of
       // q_lat or TMA zeros and are zeroed here.
-      const uint32_t qs = base + 2 * kStageBytes;
+      const uint32_t qs = base + kStageBytes;
       if (h == 0 && j == 0) {
         mbar_expect_tx(bar(B_QTMA), 4 * 16384 + 8192);
         for (int k = 0; k < 4; ++k)
